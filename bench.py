@@ -1,0 +1,303 @@
+"""Benchmark: DeepSeekMoE layer forward on B300, one JSON line on stdout.
+
+Workload: the full-width prefill layer (T=16384 tokens, d=7168, 256 routed +
+1 shared SwiGLU experts, I=2048, top-8, 8 groups / at most 4 per token),
+synthetic seeded inputs and random-init weights. A step is one whole layer
+forward: route -> quantise -> permute -> grouped FP8 GEMM (gate/up, SwiGLU,
+requantise) -> grouped FP8 GEMM (down) -> combine -> bias update.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config full]
+  python bench.py --impl reference ...   # the FP64 CPU oracle on a token sample
+
+Under torchrun (N > 1) each rank runs its own layer on its own tokens (weak
+scaling); the only exchange is an all-reduce of the per-expert load before
+the bias update. value = tokens of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s; FP8 grouped-GEMM TFLOP/s & % of roofline (1 B300)"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6400.0), d.get("bf16_tflops", 1800.0), d.get("bf16_tflops_sustained"), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    from sparse_moe_layer_13_b300 import binding, inputs
+    from sparse_moe_layer_13_b300.configs import CONFIGS
+    from sparse_moe_layer_13_b300.layer import MoELayer
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    if ws > 1:
+        dist.barrier()
+    cfg = CONFIGS[args.config]
+    layer = MoELayer(cfg, dev)
+    # each rank its own tokens: a different x batch per rank
+    x = inputs.gen_x(cfg, dev, step=rank)
+    hook = (lambda c: dist.all_reduce(c)) if ws > 1 else None
+    # bias update counts the whole data-parallel batch: scale T by ranks
+    T_all = cfg.T * ws
+
+    def _step(events=None):
+        y = layer.forward(x, update_bias=False, events=events)
+        if hook is not None:
+            hook(layer.counts)
+        binding.bias_update(cfg.E, T_all, cfg.K, layer.counts, cfg.gamma, layer.bias)
+        return y
+
+    for _ in range(args.warmup):
+        _step()
+    torch.cuda.synchronize()
+    binding.check_device_status()
+
+    K = args.steps
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for n in ("gemm1", "gemm2")}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0.record()
+        for i in range(K):
+            _step({n: ev[n][i] for n in ev})
+        t1.record()
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+    binding.check_device_status()
+    ms = t0.elapsed_time(t1) / K
+    g1 = statistics.mean(a.elapsed_time(b) for a, b in ev["gemm1"])
+    g2 = statistics.mean(a.elapsed_time(b) for a, b in ev["gemm2"])
+    if ws > 1:
+        t = torch.tensor([ms, g1, g2], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, g1, g2 = t.tolist()
+
+    # end to end through the public API: pinned host x in, host y out, every step
+    xh = x.cpu().pin_memory()
+    yh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        xd.copy_(xh, non_blocking=True)
+        y = layer.forward(xd, update_bias=False)
+        if hook is not None:
+            hook(layer.counts)
+        binding.bias_update(cfg.E, T_all, cfg.K, layer.counts, cfg.gamma, layer.bias)
+        yh.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+
+    hbm, bf16, bf16_s, src = _peaks()
+    f1, f2 = cfg.gemm_flops()
+    fp8_peak = 2.0 * bf16          # E4M3 dense rate is twice bf16 (4.5 vs 2.25 PFLOP/s nominal)
+    g1_tflops = f1 / (g1 * 1e-3) / 1e12
+    g2_tflops = f2 / (g2 * 1e-3) / 1e12
+    tokens = cfg.T * ws
+    value = tokens / (ms * 1e-3)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic (seeded N(0,1) x, N(0,1/d) weights, random init)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E}+1 I={cfg.I} K={cfg.K} G={cfg.G} M={cfg.M}",
+                   "tokens_per_gpu": cfg.T, "global_tokens": tokens, "parallelism": f"dp{ws}",
+                   "l2": "inputs exceed L2 (x 235 MB, FP8 weights 11.3 GB per step)"},
+        "layer_tflops": round(cfg.flops() * ws / (ms * 1e-3) / 1e12, 1),
+        "gemm": {"gate_up_swiglu_ms": round(g1, 4), "gate_up_tflops": round(g1_tflops, 1),
+                 "down_ms": round(g2, 4), "down_tflops": round(g2_tflops, 1),
+                 "grouped_gemm_tflops": round((f1 + f2) / ((g1 + g2) * 1e-3) / 1e12, 1)},
+        "roofline": {"kernel": "grouped_gemm_fp8 gate/up + SwiGLU (largest share of the step)",
+                     "bound": "tensor", "achieved": round(g1_tflops, 1), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(g1_tflops / fp8_peak, 4), "traffic": None,
+                     "peak_source": f"{src}: bf16 burst {bf16} TFLOP/s x 2 (E4M3/bf16 nominal ratio)"},
+        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2},
+        "gpu_launches": K * layer.LAUNCHES_PER_FORWARD,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, n_tokens=args.cpu_tokens, steps=1)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(cfg, n_tokens: int, steps: int):
+    """The FP64 oracle as it stands, on a sample of n_tokens tokens of the workload.
+
+    Weight quantisation is set-up on both sides and is not timed (here it
+    runs in parallel worker processes); each step times Layer.forward on a
+    fresh sample of tokens drawn from the same seeded batch.
+    """
+    import numpy as np
+    import torch
+
+    from oracle.layer import Layer
+    from oracle.parallel import quantize_experts
+    from oracle.route import route as oracle_route
+    from sparse_moe_layer_13_b300 import inputs
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = inputs.gen_x(cfg, dev).float().cpu().numpy()
+    Wr = inputs.gen_router(cfg, dev).cpu().numpy()
+    b = inputs.gen_bias(cfg, dev).cpu().numpy()
+    rng = np.random.default_rng(1234)
+    samples = [np.sort(rng.choice(cfg.T, n_tokens, replace=False)) for _ in range(steps)]
+    idx, _, _ = oracle_route(x[np.concatenate(samples)], Wr, b, cfg.G, cfg.M, cfg.K, cfg.gk)
+    need = sorted(set(idx.ravel().tolist()) | {cfg.E})
+    ex = quantize_experts((e, *(w.cpu().numpy() for w in inputs.gen_expert(cfg, e, dev))) for e in need)
+    layer = Layer(cfg, Wr, b, None, experts=ex)
+    threads = torch.get_num_threads()
+    t = time.perf_counter()
+    for s in samples:
+        layer.forward(x[s])
+    dt = time.perf_counter() - t
+    from threadpoolctl import threadpool_info
+    blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    return {"value": round(n_tokens * steps / dt, 4), "unit": UNIT, "cores": blas, "kind": "oracle",
+            "sample": f"{n_tokens * steps} tokens of the {cfg.name} batch (whole layer per token: route, "
+                      f"quantise, {cfg.K}+1 expert FFNs in FP64, combine); weight quantisation untimed",
+            "host_cpus": os.cpu_count(), "torch_threads": threads}
+
+
+def run_reference(args):
+    """--impl reference: the oracle itself, timed on the host cores, same metric and config."""
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    from sparse_moe_layer_13_b300.configs import CONFIGS
+    cfg = CONFIGS[args.config]
+    n = max(1, args.ref_tokens)
+    # warm-up steps run the same sampled forward untimed inside cpu_baseline's single pass
+    cb = cpu_baseline(cfg, n_tokens=n, steps=max(1, args.steps))
+    ms = 1e3 * n / cb["value"]
+    out = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E}+1 I={cfg.I} K={cfg.K} G={cfg.G} M={cfg.M}"},
+           "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+           "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="full")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=4)
+    ap.add_argument("--ref-tokens", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

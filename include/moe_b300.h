@@ -1,0 +1,217 @@
+/*
+ * moe_b300.h -- C ABI of the B300 (sm_103a) DeepSeekMoE layer forward.
+ *
+ * The layer (《DeepSeek-V3 Technical Report》深度解读报告, §2.2 DeepSeekMoE):
+ *     y = [u +] FFN_shared(u) + sum_{k<K} g_k * FFN_{e_k}(u)
+ * with sigmoid affinities, aux-loss-free biased top-K choice (§2.3),
+ * group-limited routing (§2.4), and expert FFNs run as FP8 (E4M3) GEMMs
+ * with activations scaled per 1x128 tile, weights per 128x128 block and
+ * partial sums promoted to FP32 every 128-element K chunk ("DeepSeek-V3的
+ * MoE架构设计革新", §2 FP8 training, items 1-2).
+ *
+ * Conventions for every call:
+ *  - The caller owns all memory. Pointers named as device pointers must be
+ *    device memory of the current CUDA device; the library never
+ *    allocates. Calls that need scratch take a caller-provided workspace of
+ *    at least moe_workspace_size() bytes.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) except where stated. Calls never print, never
+ *    throw and never abort.
+ *  - Errors found on the host (null pointer, bad size, misalignment, too
+ *    small workspace) return a non-zero status before anything is launched.
+ *    Errors found on the device (corrupt routing indices or offsets, a
+ *    bounded wait that ran out) set a device status word that
+ *    moe_check_device_status() reads and clears.
+ *  - bf16 tensors are passed as uint16_t bit patterns. Matrices are
+ *    row-major with the last index contiguous unless stated.
+ *  - Device pointers must be 16-byte aligned.
+ *
+ * Shapes (moe_config): T tokens, d hidden, E routed experts, I expert
+ * intermediate size (the shared expert has the same I), K experts per
+ * token, G expert groups (contiguous blocks of E/G experts standing in for
+ * nodes), M groups a token may reach, gk highest affinities summed into a
+ * group's score. Supported: T >= 1; d, I multiples of 128; 16 <= E <= 1024,
+ * E % 16 == 0, E % G == 0, G <= 32; 1 <= M <= G; 1 <= gk <= E/G;
+ * 1 <= K <= min(16, M*E/G). Anything else is MOE_ERR_UNSUPPORTED_SHAPE.
+ *
+ * Grouped rows: the routed (token, slot) pairs are grouped by expert
+ * (ascending expert, then ascending token) into rows [0, T*K); the shared
+ * expert's rows T*K + t (t < T) follow, so the whole layer runs as one
+ * grouped GEMM over E + 1 groups.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,       /* null or misaligned pointer, negative size, bad enum */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above */
+    MOE_ERR_WORKSPACE = 3,         /* workspace missing or smaller than required */
+    MOE_ERR_CUDA = 4,              /* a CUDA runtime call failed (see cudaGetLastError) */
+    MOE_ERR_TIMEOUT = 5,           /* a bounded device wait ran out; kernel returned early */
+    MOE_ERR_DEVICE_CHECK = 6,      /* a device-side check of indices or offsets failed */
+    MOE_ERR_NO_DEVICE = 7          /* no usable sm_103 device is current */
+} moe_status;
+
+typedef struct moe_config {
+    int32_t T, d, E, I, K, G, M, gk;
+} moe_config;
+
+/* Epilogues of the grouped FP8 GEMM. */
+typedef enum moe_epilogue {
+    /* out: bf16 [rows][N]. */
+    MOE_EPI_BF16 = 0,
+    /* SwiGLU + 1x128 requantisation. B holds gate (W1) and up (W3) rows
+     * interleaved as moe_pack_w13 writes them; out: E4M3 [rows][N/2],
+     * out_scale: f32 [rows][N/256]. */
+    MOE_EPI_SWIGLU_FP8 = 1
+} moe_epilogue;
+
+/* Human-readable name of a status. Never NULL. */
+const char* moe_status_string(moe_status s);
+
+/* Version string of the library build. */
+const char* moe_version(void);
+
+/* Synchronises `stream`, then returns and clears the device status word
+ * (MOE_OK if no device-side check failed since the last call). Blocking. */
+moe_status moe_check_device_status(void* stream);
+
+/* Bytes of workspace moe_route and moe_permute need for `cfg` (the larger
+ * of the two). 0 for an unsupported cfg. Host only, no device access. */
+size_t moe_workspace_size(const moe_config* cfg);
+
+/* Router: affinity, aux-loss-free group-limited top-K and gates.
+ * 《DeepSeek-V3 Technical Report》深度解读报告 §2.2 (s_e = sigmoid(x . Wr_e),
+ * gates = s over the chosen experts renormalised to 1), §2.3 (b_e added to
+ * s_e only to choose experts), §2.4 (at most M groups per token, groups
+ * ranked by the sum of their gk highest biased affinities).
+ *   x            device bf16 [T][d]
+ *   Wr           device f32  [E][d]
+ *   logit_offset device f32  [E] or NULL: added to x . Wr_e before the sigmoid
+ *                (a synthetic knob that skews expert popularity)
+ *   bias         device f32  [E] selection bias b
+ *   topk_idx     device i32  [T][K] out: chosen experts, by descending s + b
+ *                (equal values: lower expert index first)
+ *   topk_gate    device f32  [T][K] out: s_e / sum of s over the chosen experts
+ *   counts       device i32  [E] out or NULL: pairs routed to each expert
+ *   workspace    device, >= moe_workspace_size(cfg) bytes
+ * Logits are computed on the tensor cores from x (bf16, exact) times Wr
+ * split into three bf16 terms whose sum is Wr exactly, accumulated in FP32. */
+moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr,
+                     const float* logit_offset, const float* bias,
+                     int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Activation quantisation per 1x128 tile ("DeepSeek-V3的MoE架构设计革新" §2
+ * item 1; E4M3 largest finite value 448 from "DeepSeek-V3技术解析" §6.2):
+ *   scale = fl32(amax / 448); q = E4M3_RNE_SATFINITE(fl32(x / scale)),
+ *   scale 0 and codes 0x00/0x80 (by sign) for an all-zero tile.
+ *   x     device bf16 [rows][ld] (the first cols of each row are used)
+ *   q     device u8   [rows][cols]
+ *   scale device f32  [rows][cols/128]
+ * cols % 128 == 0, ld >= cols, ld % 8 == 0. */
+moe_status moe_quant_fp8_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                               uint8_t* q, float* scale, void* stream);
+
+/* Weight quantisation per 128x128 block, same rule as above with amax over
+ * the block (same page, same item). Set-up only; `batch` independent
+ * matrices stored back to back.
+ *   w     device f32 [batch][rows][cols]
+ *   q     device u8  [batch][rows][cols]
+ *   scale device f32 [batch][rows/128][cols/128]
+ * rows % 128 == 0, cols % 128 == 0. */
+moe_status moe_quant_fp8_128x128(const float* w, int64_t batch, int64_t rows, int64_t cols,
+                                 uint8_t* q, float* scale, void* stream);
+
+/* Lays out quantised gate (W1) and up (W3) projections for the SwiGLU
+ * epilogue. For each 128-row block j of I, rows 256j + [0,64) of W13 are
+ * W1 rows 128j + [0,64), then W3 rows 128j + [0,64), then W1 rows
+ * 128j + [64,128), then W3 rows 128j + [64,128). Scales: block 2j of the
+ * output is W1's block j, block 2j + 1 is W3's block j.
+ *   q1, q3   device u8  [batch][I][d];  s1, s3 device f32 [batch][I/128][d/128]
+ *   q13      device u8  [batch][2I][d]; s13    device f32 [batch][2I/128][d/128]
+ * Set-up only. */
+moe_status moe_pack_w13(const uint8_t* q1, const float* s1, const uint8_t* q3, const float* s3,
+                        int64_t batch, int64_t I, int64_t d,
+                        uint8_t* q13, float* s13, void* stream);
+
+/* Token permutation by expert (expert histogram, exclusive prefix sum and a
+ * stable scatter, all without atomics), then a gather of the quantised
+ * rows into grouped order. Rows are ordered by (expert, token); the shared
+ * expert's rows T*K + t follow.
+ *   topk_idx     device i32 [T][K] (values in [0, E); else MOE_ERR_DEVICE_CHECK)
+ *   xq, xs       device u8 [T][d], f32 [T][d/128] (moe_quant_fp8_1x128 of x)
+ *   offsets      device i32 [E+2] out: group g holds rows [offsets[g], offsets[g+1]);
+ *                group E is the shared expert (offsets[E] = T*K, offsets[E+1] = T*K + T)
+ *   counts       device i32 [E] out or NULL: histogram of topk_idx
+ *   sorted_token device i32 [T*K] out: token of each routed row
+ *   row_of       device i32 [T][K] out: grouped row of each (token, slot)
+ *   xq_perm      device u8  [T*K + T][d] out
+ *   xs_perm      device f32 [T*K + T][d/128] out
+ *   workspace    device, >= moe_workspace_size(cfg) bytes */
+moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx,
+                       const uint8_t* xq, const float* xs,
+                       int32_t* offsets, int32_t* counts, int32_t* sorted_token, int32_t* row_of,
+                       uint8_t* xq_perm, float* xs_perm,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Grouped FP8 GEMM with per-chunk scale promotion
+ * ("DeepSeek-V3的MoE架构设计革新" §2 items 1-2): for each group g and row r in
+ * [offsets[g], offsets[g+1]),
+ *   D[r][n] = sum_kc sa[r][kc] * sb[g][n/128][kc] * sum_{k in chunk kc} A[r][k] * B[g][n][k]
+ * with E4M3 A and B, FP32 accumulation, kc over Kdim/128 chunks.
+ *   groups    number of groups (<= 1025)
+ *   offsets   device i32 [groups+1], non-decreasing, offsets[groups] <= rows
+ *             (checked on the device: MOE_ERR_DEVICE_CHECK, nothing written)
+ *   rows      rows of A and of the output
+ *   A, sa     device u8 [rows][Kdim], f32 [rows][Kdim/128]
+ *   B, sb     device u8 [groups][N][Kdim], f32 [groups][N/128][Kdim/128]
+ *   epilogue  moe_epilogue; out / out_scale as described there
+ * N % 256 == 0, Kdim % 128 == 0. Rows outside every group are not written.
+ * Runs on the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA
+ * operand loads); no workspace. */
+moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t rows,
+                                int32_t N, int32_t Kdim,
+                                const uint8_t* A, const float* sa,
+                                const uint8_t* B, const float* sb,
+                                int32_t epilogue, void* out, float* out_scale, void* stream);
+
+/* Gate-weighted un-permute and combine (《DeepSeek-V3 Technical Report》深度解读报告
+ * §2.2): y[t] = shared_out[t] + sum_k topk_gate[t][k] * routed_out[row_of[t][k]]
+ * (+ residual[t] if residual != NULL), accumulated in FP32 in that order,
+ * rounded to bf16.
+ *   routed_out device bf16 [T*K][d]; shared_out device bf16 [T][d]
+ *   row_of     device i32 [T][K] (values in [0, T*K), else MOE_ERR_DEVICE_CHECK)
+ *   topk_gate  device f32 [T][K]; residual device bf16 [T][d] or NULL
+ *   y          device bf16 [T][d] out */
+moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const uint16_t* shared_out,
+                       const int32_t* row_of, const float* topk_gate, const uint16_t* residual,
+                       uint16_t* y, void* stream);
+
+/* End-of-step bias update (《DeepSeek-V3 Technical Report》深度解读报告 §2.3):
+ *   b_e <- fl32(b_e + gamma * sign(T*K/E - counts[e]))
+ * i.e. overloaded experts lose gamma, underloaded experts gain gamma, an
+ * expert exactly at the mean load keeps its bias.
+ *   counts device i32 [E]; bias device f32 [E] in/out. */
+moe_status moe_bias_update(int32_t E, int32_t T, int32_t K, const int32_t* counts,
+                           float gamma, float* bias, void* stream);
+
+/* Failure-detection self test: launches one kernel that waits, with a
+ * limit of `limit_us` microseconds, on a barrier nothing will complete, and
+ * reports through the device status word. Returns MOE_ERR_TIMEOUT (after a
+ * stream synchronisation) when the bounded wait behaves. Blocking. */
+moe_status moe_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

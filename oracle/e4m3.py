@@ -44,7 +44,33 @@ def decode(codes) -> np.ndarray:
 
 
 def encode(v) -> np.ndarray:
-    """float32 values -> uint8 codes, round-to-nearest-even, saturating at 448."""
+    """float32 values -> uint8 codes, round-to-nearest-even, saturating at 448.
+
+    Rounds the magnitude a (clamped to 448) to a multiple of the E4M3 spacing
+    of its binade, 2^(e-3) with e = max(floor(log2 a), -6); the multiple is
+    chosen by round-half-to-even, which is the even-mantissa tie rule. The
+    binade exponent is read from the float32 bit pattern; every division
+    and product here is by a power of two, so it is exact.
+    """
+    v = np.asarray(v, dtype=np.float32)
+    a = np.minimum(np.abs(v), np.float32(E4M3_MAX))
+    e = ((a.view(np.uint32) >> 23).astype(np.int32) - 127)
+    e = np.maximum(e, -6)
+    spacing = ((e + (127 - 3)).astype(np.uint32) << 23).view(np.float32)
+    r = np.round(a / spacing)                          # half to even
+    val = r * spacing
+    vb = val.view(np.uint32)
+    normal = val >= np.float32(2.0 ** -6)
+    exp_field = np.where(normal, (vb >> 23).astype(np.int32) - 127 + 7, 0)
+    man_field = np.where(normal, (vb >> 20) & 7, r.astype(np.int32))
+    code = (exp_field << 3) | man_field
+    code = np.where(np.signbit(v), code | 0x80, code)
+    code = np.where(np.isnan(v), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def encode_by_search(v) -> np.ndarray:
+    """Same result as encode(), by nearest-neighbour search in the code table."""
     v = np.asarray(v, dtype=np.float32)
     a = np.abs(v.astype(np.float64))
     neg = np.signbit(v)

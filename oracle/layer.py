@@ -44,16 +44,17 @@ class Layer:
     """Oracle for one layer instance.
 
     expert_weights(e) -> (W1 [I][d], W3 [I][d], W2 [d][I]) float32, with e == E
-    the shared expert. Quantised experts are built on first use and cached.
+    the shared expert. Quantised experts are built on first use and cached;
+    `experts` may pre-fill that cache with QuantExpert objects.
     """
 
-    def __init__(self, cfg, Wr, bias, expert_weights, logit_offset=None):
+    def __init__(self, cfg, Wr, bias, expert_weights, logit_offset=None, experts=None):
         self.cfg = cfg
         self.Wr = np.asarray(Wr, np.float32)
         self.bias = np.asarray(bias, np.float32)
         self.logit_offset = None if logit_offset is None else np.asarray(logit_offset, np.float32)
         self._weights = expert_weights
-        self._experts: dict[int, QuantExpert] = {}
+        self._experts: dict[int, QuantExpert] = dict(experts or {})
 
     def expert(self, e: int) -> QuantExpert:
         if e not in self._experts:

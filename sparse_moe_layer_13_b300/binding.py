@@ -1,0 +1,228 @@
+"""ctypes binding of libmoe_b300.so (C ABI declared in include/moe_b300.h).
+
+Argument marshalling only: every wrapper checks dtypes, devices and
+contiguity, allocates outputs with torch when the caller gives none, and
+passes raw pointers plus the current CUDA stream to the library. There is
+no fallback: if the shared library is missing or cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_NAME = "libmoe_b300.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
+
+MOE_EPI_BF16 = 0
+MOE_EPI_SWIGLU_FP8 = 1
+
+STATUS = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE",
+    4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_CHECK", 7: "MOE_ERR_NO_DEVICE",
+}
+
+# name -> (restype, argtypes)
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SIG = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_version": (ctypes.c_char_p, []),
+    "moe_check_device_status": (ctypes.c_int, [_P]),
+    "moe_workspace_size": (ctypes.c_size_t, [_P]),
+    "moe_route": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_quant_fp8_1x128": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P]),
+    "moe_quant_fp8_128x128": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P]),
+    "moe_pack_w13": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "moe_permute": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_grouped_gemm_fp8": (ctypes.c_int, [_I32, _P, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P]),
+    "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_bias_update": (ctypes.c_int, [_I32, _I32, _I32, _P, ctypes.c_float, _P, _P]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
+}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class MoEConfigC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "d", "E", "I", "K", "G", "M", "gk")]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library once; raise if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{LIB_NAME} is not built ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIG.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _call(name: str, *args) -> None:
+    rc = getattr(load(), name)(*args)
+    if rc != 0:
+        raise MoeError(name, rc)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str, shape=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous CUDA {dtype} tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def config_c(cfg) -> MoEConfigC:
+    return MoEConfigC(*cfg.abi())
+
+
+def version() -> str:
+    return load().moe_version().decode()
+
+
+def check_device_status() -> None:
+    rc = load().moe_check_device_status(_stream())
+    if rc != 0:
+        raise MoeError("device status", rc)
+
+
+def selftest_wait_timeout(limit_us: int) -> int:
+    return load().moe_selftest_wait_timeout(limit_us, _stream())
+
+
+def workspace_size(cfg) -> int:
+    c = config_c(cfg)
+    return load().moe_workspace_size(ctypes.byref(c))
+
+
+def route(cfg, x, Wr, bias, logit_offset=None, workspace=None, idx=None, gate=None, counts=None, want_counts=False):
+    dev = x.device
+    _need(x, torch.bfloat16, "x", (cfg.T, cfg.d))
+    _need(Wr, torch.float32, "Wr", (cfg.E, cfg.d))
+    _need(bias, torch.float32, "bias", (cfg.E,))
+    if logit_offset is not None:
+        _need(logit_offset, torch.float32, "logit_offset", (cfg.E,))
+    idx = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev) if idx is None else idx
+    gate = torch.empty(cfg.T, cfg.K, dtype=torch.float32, device=dev) if gate is None else gate
+    if want_counts and counts is None:
+        counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_size(cfg), dtype=torch.uint8, device=dev)
+    c = config_c(cfg)
+    _call("moe_route", ctypes.byref(c), _ptr(x), _ptr(Wr), _ptr(logit_offset), _ptr(bias), _ptr(idx), _ptr(gate),
+          _ptr(counts), _ptr(workspace), workspace.numel(), _stream())
+    return idx, gate, counts
+
+
+def quant_1x128(x, q=None, scale=None):
+    _need(x, torch.bfloat16, "x")
+    rows, cols = x.shape
+    q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device) if q is None else q
+    scale = torch.empty(rows, cols // 128, dtype=torch.float32, device=x.device) if scale is None else scale
+    _call("moe_quant_fp8_1x128", _ptr(x), rows, cols, cols, _ptr(q), _ptr(scale), _stream())
+    return q, scale
+
+
+def quant_128x128(w, q=None, scale=None):
+    """w float32 [rows][cols] or [batch][rows][cols]."""
+    _need(w, torch.float32, "w")
+    w3 = w if w.dim() == 3 else w.unsqueeze(0)
+    b, rows, cols = w3.shape
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device) if q is None else q
+    sshape = (rows // 128, cols // 128) if w.dim() == 2 else (b, rows // 128, cols // 128)
+    scale = torch.empty(sshape, dtype=torch.float32, device=w.device) if scale is None else scale
+    _call("moe_quant_fp8_128x128", _ptr(w), b, rows, cols, _ptr(q), _ptr(scale), _stream())
+    return q, scale
+
+
+def pack_w13(q1, s1, q3, s3, q13=None, s13=None):
+    """q1, q3 u8 [batch][I][d]; s1, s3 f32 [batch][I/128][d/128] -> W13 in the SwiGLU epilogue layout."""
+    b, I, d = q1.shape
+    q13 = torch.empty(b, 2 * I, d, dtype=torch.uint8, device=q1.device) if q13 is None else q13
+    s13 = torch.empty(b, 2 * I // 128, d // 128, dtype=torch.float32, device=q1.device) if s13 is None else s13
+    _call("moe_pack_w13", _ptr(q1), _ptr(s1), _ptr(q3), _ptr(s3), b, I, d, _ptr(q13), _ptr(s13), _stream())
+    return q13, s13
+
+
+def permute(cfg, idx, xq, xs, workspace=None, out=None, want_counts=False):
+    dev = idx.device
+    _need(idx, torch.int32, "topk_idx", (cfg.T, cfg.K))
+    _need(xq, torch.uint8, "xq", (cfg.T, cfg.d))
+    _need(xs, torch.float32, "xs", (cfg.T, cfg.d // 128))
+    rows = cfg.rows
+    if out is None:
+        out = {
+            "offsets": torch.empty(cfg.E + 2, dtype=torch.int32, device=dev),
+            "counts": torch.empty(cfg.E, dtype=torch.int32, device=dev) if want_counts else None,
+            "sorted_token": torch.empty(cfg.T * cfg.K, dtype=torch.int32, device=dev),
+            "row_of": torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev),
+            "xq_perm": torch.empty(rows, cfg.d, dtype=torch.uint8, device=dev),
+            "xs_perm": torch.empty(rows, cfg.d // 128, dtype=torch.float32, device=dev),
+        }
+    if workspace is None:
+        workspace = torch.empty(workspace_size(cfg), dtype=torch.uint8, device=dev)
+    c = config_c(cfg)
+    _call("moe_permute", ctypes.byref(c), _ptr(idx), _ptr(xq), _ptr(xs), _ptr(out["offsets"]), _ptr(out["counts"]),
+          _ptr(out["sorted_token"]), _ptr(out["row_of"]), _ptr(out["xq_perm"]), _ptr(out["xs_perm"]),
+          _ptr(workspace), workspace.numel(), _stream())
+    return out
+
+
+def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out_scale=None):
+    """offsets i32 [G+1]; A u8 [rows][K]; sa f32 [rows][K/128]; B u8 [G][N][K]; sb f32 [G][N/128][K/128]."""
+    groups = offsets.numel() - 1
+    rows, Kdim = A.shape
+    N = B.shape[1]
+    _need(offsets, torch.int32, "offsets")
+    _need(A, torch.uint8, "A")
+    _need(sa, torch.float32, "sa", (rows, Kdim // 128))
+    _need(B, torch.uint8, "B", (groups, N, Kdim))
+    _need(sb, torch.float32, "sb", (groups, N // 128, Kdim // 128))
+    if epilogue == MOE_EPI_BF16:
+        out = torch.empty(rows, N, dtype=torch.bfloat16, device=A.device) if out is None else out
+    else:
+        out = torch.empty(rows, N // 2, dtype=torch.uint8, device=A.device) if out is None else out
+        out_scale = (torch.empty(rows, N // 256, dtype=torch.float32, device=A.device)
+                     if out_scale is None else out_scale)
+    _call("moe_grouped_gemm_fp8", groups, _ptr(offsets), rows, N, Kdim, _ptr(A), _ptr(sa), _ptr(B), _ptr(sb),
+          epilogue, _ptr(out), _ptr(out_scale), _stream())
+    return out, out_scale
+
+
+def combine(cfg, routed_out, shared_out, row_of, gate, residual=None, y=None):
+    y = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=row_of.device) if y is None else y
+    c = config_c(cfg)
+    _call("moe_combine", ctypes.byref(c), _ptr(routed_out), _ptr(shared_out), _ptr(row_of), _ptr(gate),
+          _ptr(residual), _ptr(y), _stream())
+    return y
+
+
+def bias_update(E, T, K, counts, gamma, bias):
+    _need(counts, torch.int32, "counts", (E,))
+    _need(bias, torch.float32, "bias", (E,))
+    _call("moe_bias_update", E, T, K, _ptr(counts), ctypes.c_float(gamma), _ptr(bias), _stream())
+    return bias

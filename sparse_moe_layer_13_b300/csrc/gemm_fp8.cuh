@@ -1,0 +1,316 @@
+// Grouped FP8 GEMM with fine-grained scales on the 5th-generation tensor
+// cores ("DeepSeek-V3的MoE架构设计革新" §2 FP8 training: activations scaled per
+// 1x128 tile, weights per 128x128 block, partial sums promoted to FP32 at
+// every 128-element K chunk).
+//
+// Persistent, warp-specialised kernel, one CTA per SM:
+//   warp 0      TMA producer: A tile 128x128 and B tile 256x128 (E4M3,
+//               128-byte swizzle) per K chunk into a 4-stage ring.
+//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=32) per chunk
+//               into one of two TMEM chunk accumulators (2 x 256 columns).
+//   warps 2,3   idle (they complete the first warpgroup, which gives its
+//               registers to the epilogue warpgroups via setmaxnreg)
+//   warps 4..11 epilogue: per chunk, tcgen05.ld the 128x256 FP32 partial,
+//               multiply by sa[row][kc] * sb[group][n/128][kc] and add to
+//               the FP32 tile accumulator kept in registers (128 values per
+//               thread: lane quadrant = warp % 4, column half = (warp-4)/4).
+//               After the last chunk: bf16 store, or SwiGLU + 1x128 E4M3
+//               requantisation of h.
+// The chunk accumulator is released as soon as it is read, so the tensor
+// cores run up to two chunks ahead of the promotion arithmetic.
+//
+// Tiles: for each group, ceil(m_g / 128) row tiles x N/256 column tiles,
+// numbered group by group with the column tile fastest; CTA c takes tiles
+// c, c + gridDim.x, ... A rows past a group's end belong to the next group
+// (or are TMA zero fill past the last row); their results are never stored.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 384;
+// Register split: launch budget 384 x 168 = 64512. The producer warpgroup
+// drops to 40 per thread (128 x 40 = 5120), the two epilogue warpgroups
+// rise to 232 (256 x 232 = 59392); 5120 + 59392 = 64512.
+constexpr uint32_t kRegsProducer = 40;
+constexpr uint32_t kRegsEpilogue = 232;
+constexpr int MAX_GROUPS = 1025;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC = make_idesc(BM, BN, 0);
+
+struct Smem {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t mma_done;
+    uint64_t pair[4];                 // SwiGLU amax exchange between the two warps of a lane quadrant
+    uint32_t tmem_base;
+    int abort;
+    int bad;
+    int mtiles_total;
+    int row_start[MAX_GROUPS + 1];    // offsets[g]
+    int mtile_prefix[MAX_GROUPS + 1]; // exclusive prefix of ceil(m_g / BM)
+    float amax_x[2][8][32];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Smem);
+
+struct Params {
+    const int32_t* offsets;
+    int32_t groups;
+    int64_t rows;
+    int32_t N;
+    int32_t Kdim;
+    const float* sa;
+    const float* sb;
+    void* out;
+    float* out_scale;
+};
+
+// tile -> (group, row tile inside the group, column tile)
+__device__ __forceinline__ void decode_tile(const Smem& s, int groups, int ntiles, int tile, int& g, int& mt, int& nt) {
+    const int mtg = tile / ntiles;
+    nt = tile - mtg * ntiles;
+    int lo = 0, hi = groups - 1;           // last g with mtile_prefix[g] <= mtg
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.mtile_prefix[mid] <= mtg) lo = mid; else hi = mid - 1;
+    }
+    g = lo;
+    mt = mtg - s.mtile_prefix[g];
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = base;
+    uint8_t* sB = base + STAGES * A_BYTES;
+    Smem& s = *reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
+    const int groups = p.groups;
+    const int ntiles = p.N / BN;
+    const int nkc = p.Kdim / BK;
+
+    // ---- set-up: barriers, TMEM, per-group row tiles -------------------------
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&s.tfull[i], 1); mbar_init(&s.tempty[i], 8); }
+        mbar_init(&s.mma_done, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&s.pair[i], 64);
+        s.abort = 0;
+        s.bad = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&s.tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    for (int g = threadIdx.x; g <= groups; g += NUM_THREADS) s.row_start[g] = __ldg(p.offsets + g);
+    __syncthreads();
+    for (int g = threadIdx.x; g < groups; g += NUM_THREADS) {
+        const int a = s.row_start[g], b = s.row_start[g + 1];
+        if (a < 0 || b < a || static_cast<int64_t>(b) > p.rows) s.bad = 1;
+    }
+    __syncthreads();
+    if (warp == 2) {
+        int carry = 0;
+        for (int b0 = 0; b0 < groups; b0 += 32) {
+            const int g = b0 + static_cast<int>(lane);
+            int v = 0;
+            if (g < groups && !s.bad) v = (s.row_start[g + 1] - s.row_start[g] + BM - 1) / BM;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (static_cast<int>(lane) >= o) incl += t;
+            }
+            if (g < groups) s.mtile_prefix[g] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            s.mtile_prefix[groups] = carry;
+            s.mtiles_total = carry;
+            if (s.bad && blockIdx.x == 0) set_status(MOE_ERR_DEVICE_CHECK);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s.tmem_base;
+    const int total = s.mtiles_total * ntiles;
+    volatile int* abort = &s.abort;
+
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
+      if (warp == 0) {
+        // ---------------------------------------------------- TMA producer ----
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+                int g, mt, nt;
+                decode_tile(s, groups, ntiles, tile, g, mt, nt);
+                const int row0 = s.row_start[g] + mt * BM;
+                const int brow = g * p.N + nt * BN;
+                for (int kc = 0; kc < nkc; ++kc, ++it) {
+                    const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(&s.empty[st], ph ^ 1u, abort, kWaitLimitNs)) break;
+                    mbar_expect_tx(&s.full[st], STAGE_BYTES);
+                    tma_load_2d(sA + st * A_BYTES, &tmA, &s.full[st], kc * BK, row0);
+                    tma_load_2d(sB + st * B_BYTES, &tmB, &s.full[st], kc * BK, brow);
+                }
+            }
+            if (*abort) {
+                // let every issued copy land before the CTA exits
+                const uint32_t first = it > STAGES ? it - STAGES : 0;
+                for (uint32_t j = first; j < it; ++j)
+                    mbar_wait(&s.full[j % STAGES], (j / STAGES) & 1u, nullptr, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer ----
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+                for (int kc = 0; kc < nkc; ++kc, ++it) {
+                    const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
+                    const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+                    if (!mbar_wait(&s.tempty[b], bph ^ 1u, abort, kWaitLimitNs)) break;
+                    if (!mbar_wait(&s.full[st], ph, abort, kWaitLimitNs)) break;
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(smem_addr(sA + st * A_BYTES));
+                    const uint64_t bd = sw128_desc(smem_addr(sB + st * B_BYTES));
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_e4m3(tmem + b * BN, ad + 2 * k, bd + 2 * k, IDESC, k > 0 ? 1u : 0u);
+                    tc_commit(&s.empty[st]);
+                    tc_commit(&s.tfull[b]);
+                }
+            }
+            // no MMA may be in flight when TMEM is released
+            tc_commit(&s.mma_done);
+            mbar_wait(&s.mma_done, 0, nullptr, kWaitLimitNs);
+        }
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpilogue));
+        // -------------------------------------------------------- epilogue ----
+        const int ew = warp - 4;             // 0..7
+        const int q = warp & 3;              // TMEM lane quadrant this warp may access
+        const int half = ew >> 2;            // column half of the 256-wide tile
+        const int rit = q * 32 + static_cast<int>(lane);
+        const int nbn = p.N / 128;
+        uint32_t it = 0, tcount = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
+            int g, mt, nt;
+            decode_tile(s, groups, ntiles, tile, g, mt, nt);
+            const int m_valid = s.row_start[g + 1] - s.row_start[g] - mt * BM;
+            const bool valid = rit < m_valid;
+            const int64_t row = static_cast<int64_t>(s.row_start[g]) + mt * BM + rit;
+            const float* sa_row = p.sa + (valid ? row : 0) * nkc;
+            // weight scale rows: SwiGLU -> gate block 2*nt, up block 2*nt+1; bf16 -> block 2*nt+half
+            const float* sb0 = p.sb + (static_cast<int64_t>(g) * nbn + 2 * nt + (EPI == MOE_EPI_SWIGLU_FP8 ? 0 : half)) * nkc;
+            const float* sb1 = p.sb + (static_cast<int64_t>(g) * nbn + 2 * nt + 1) * nkc;
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int kc = 0; kc < nkc; ++kc, ++it) {
+                const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+                const float sav = valid ? __ldg(sa_row + kc) : 0.0f;
+                const float f0 = sav * __ldg(sb0 + kc);
+                const float f1 = (EPI == MOE_EPI_SWIGLU_FP8) ? sav * __ldg(sb1 + kc) : f0;
+                if (!mbar_wait(&s.tfull[b], bph, abort, kWaitLimitNs)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN + half * 128;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + r * 32, v);
+                    tmem_ld_wait();
+                    tmem_reg_fence(v);
+                    const float f = (r < 2) ? f0 : f1;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[r * 32 + i] = fmaf(f, __uint_as_float(v[i]), acc[r * 32 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.tempty[b]);
+            }
+            if (!ok) break;
+            if (EPI == MOE_EPI_BF16) {
+                if (valid) {
+                    uint16_t* dst = static_cast<uint16_t*>(p.out) + row * p.N + nt * BN + half * 128;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        uint4 w;
+                        w.x = pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]);
+                        w.y = pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]);
+                        w.z = pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]);
+                        w.w = pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]);
+                        reinterpret_cast<uint4*>(dst)[i] = w;
+                    }
+                }
+            } else {
+                // h = SiLU(gate) * up for this thread's 64 columns; gate in acc[0,64), up in acc[64,128)
+                float amax = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float gte = acc[c];
+                    const float h = __fdiv_rn(gte, 1.0f + expf(-gte)) * acc[64 + c];
+                    acc[c] = h;
+                    amax = fmaxf(amax, fabsf(h));
+                }
+                // the partner warp (same quadrant, other half) holds the other 64 columns
+                s.amax_x[tcount & 1u][ew][lane] = amax;
+                mbar_arrive(&s.pair[q]);
+                if (!mbar_wait(&s.pair[q], tcount & 1u, abort, kWaitLimitNs)) break;
+                amax = fmaxf(amax, s.amax_x[tcount & 1u][ew ^ 4][lane]);
+                const float sc = __fdiv_rn(amax, kE4M3Max);
+                if (valid) {
+                    const int I = p.N / 2;
+                    uint8_t* dst = static_cast<uint8_t*>(p.out) + row * I + nt * 128 + half * 64;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 w;
+                        w.x = e4m3x4(quant_ratio(acc[16 * i + 0], sc), quant_ratio(acc[16 * i + 1], sc),
+                                     quant_ratio(acc[16 * i + 2], sc), quant_ratio(acc[16 * i + 3], sc));
+                        w.y = e4m3x4(quant_ratio(acc[16 * i + 4], sc), quant_ratio(acc[16 * i + 5], sc),
+                                     quant_ratio(acc[16 * i + 6], sc), quant_ratio(acc[16 * i + 7], sc));
+                        w.z = e4m3x4(quant_ratio(acc[16 * i + 8], sc), quant_ratio(acc[16 * i + 9], sc),
+                                     quant_ratio(acc[16 * i + 10], sc), quant_ratio(acc[16 * i + 11], sc));
+                        w.w = e4m3x4(quant_ratio(acc[16 * i + 12], sc), quant_ratio(acc[16 * i + 13], sc),
+                                     quant_ratio(acc[16 * i + 14], sc), quant_ratio(acc[16 * i + 15], sc));
+                        reinterpret_cast<uint4*>(dst)[i] = w;
+                    }
+                    if (half == 0) p.out_scale[row * (I / 128) + nt] = sc;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace gemm
+}  // namespace moe

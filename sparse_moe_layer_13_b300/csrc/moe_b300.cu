@@ -1,0 +1,306 @@
+// C ABI of the B300 DeepSeekMoE layer forward: argument checks, launch
+// planning and kernel launches. Declarations and contracts: moe_b300.h.
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm_fp8.cuh"
+#include "misc.cuh"
+#include "permute.cuh"
+#include "quant.cuh"
+#include "route.cuh"
+
+namespace {
+
+using namespace moe;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+moe_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status check_config(const moe_config* c) {
+    if (c == nullptr) return MOE_ERR_INVALID_ARG;
+    if (c->T < 1 || c->d < 128 || c->I < 128 || c->d % 128 || c->I % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->E < 16 || c->E > 1024 || c->E % 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->G < 1 || c->G > 32 || c->E % c->G) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->M < 1 || c->M > c->G) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int n = c->E / c->G;
+    if (c->gk < 1 || c->gk > n || c->gk > route::kMaxGK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->K < 1 || c->K > 16 || c->K > c->M * n) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(c->T) * (c->K + 1) > INT32_MAX / 2) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+int num_sms() {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 148;
+    }
+    return sms;
+}
+
+// Workspace layout: [route logits f32 T*E][per-block counts i32 nblk*E]
+// [per-block bases i32 nblk*E][offsets scratch i32 E+2]
+struct WsLayout {
+    size_t logits, blk_counts, blk_base, offsets, total;
+};
+
+WsLayout ws_layout(const moe_config* c) {
+    WsLayout w{};
+    const int64_t nblk = ceil_div(c->T, perm::kTokPerBlk);
+    w.logits = 0;
+    w.blk_counts = align_up(static_cast<size_t>(c->T) * c->E * sizeof(float), 256);
+    w.blk_base = w.blk_counts + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
+    w.offsets = w.blk_base + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
+    w.total = w.offsets + align_up(static_cast<size_t>(c->E + 2) * sizeof(int32_t), 256);
+    return w;
+}
+
+// ----------------------------------------------------------- tensor maps ----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D K-major byte matrix [outer][inner], box [box_outer][128 bytes], 128-byte swizzle.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {128, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p, int64_t tiles_max,
+                       cudaStream_t st) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemm::grouped_gemm_fp8_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(gemm::SMEM_BYTES)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set = true;
+    }
+    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_max, 1)));
+    gemm::grouped_gemm_fp8_kernel<EPI><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, st>>>(ta, tb, p);
+    return launch_status();
+}
+
+const char* kStatusNames[] = {
+    "MOE_OK",
+    "MOE_ERR_INVALID_ARG: null or misaligned pointer, negative size or bad enum",
+    "MOE_ERR_UNSUPPORTED_SHAPE: shape outside the supported set",
+    "MOE_ERR_WORKSPACE: workspace missing or too small",
+    "MOE_ERR_CUDA: a CUDA runtime call failed",
+    "MOE_ERR_TIMEOUT: a bounded device wait ran out",
+    "MOE_ERR_DEVICE_CHECK: a device-side index or offset check failed",
+    "MOE_ERR_NO_DEVICE: no usable sm_103 device",
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    if (static_cast<int>(s) < 0 || static_cast<int>(s) >= static_cast<int>(sizeof(kStatusNames) / sizeof(kStatusNames[0])))
+        return "MOE_ERR_UNKNOWN";
+    return kStatusNames[s];
+}
+
+const char* moe_version(void) { return "moe_b300 1.0 (sm_103a)"; }
+
+moe_status moe_check_device_status(void* stream) {
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, moe::g_status, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(moe::g_status, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+    return static_cast<moe_status>(v);
+}
+
+size_t moe_workspace_size(const moe_config* cfg) {
+    if (check_config(cfg) != MOE_OK) return 0;
+    return ws_layout(cfg).total;
+}
+
+moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr, const float* logit_offset,
+                     const float* bias, int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    const moe_status cs = check_config(cfg);
+    if (cs != MOE_OK) return cs;
+    if (!x || !Wr || !bias || !topk_idx || !topk_gate) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wr) || !aligned16(topk_idx) || !aligned16(topk_gate)) return MOE_ERR_INVALID_ARG;
+    const WsLayout wl = ws_layout(cfg);
+    if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* z = reinterpret_cast<float*>(ws + wl.logits);
+    dim3 lg(static_cast<unsigned>(ceil_div(cfg->T, 64)), static_cast<unsigned>(ceil_div(cfg->E, 64)));
+    route::logits_simt_kernel<<<lg, 256, 0, st>>>(x, Wr, cfg->T, cfg->d, cfg->E, z);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    const size_t sel_smem = static_cast<size_t>(route::kSelWarps) * 2 * cfg->E * sizeof(float);
+    const int sel_grid = static_cast<int>(std::min<int64_t>(ceil_div(cfg->T, route::kSelWarps), 65535));
+    route::select_kernel<<<sel_grid, route::kSelWarps * 32, sel_smem, st>>>(
+        z, cfg->T, cfg->E, cfg->G, cfg->M, cfg->K, cfg->gk, logit_offset, bias, topk_idx, topk_gate);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (counts != nullptr) {
+        const int nblk = static_cast<int>(ceil_div(cfg->T, perm::kTokPerBlk));
+        int32_t* blk_counts = reinterpret_cast<int32_t*>(ws + wl.blk_counts);
+        int32_t* blk_base = reinterpret_cast<int32_t*>(ws + wl.blk_base);
+        const size_t hsm = static_cast<size_t>(perm::kWarps) * cfg->E * sizeof(int);
+        const int64_t npairs = static_cast<int64_t>(cfg->T) * cfg->K;
+        perm::hist_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E, blk_counts);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+        int32_t* offs = reinterpret_cast<int32_t*>(ws + wl.offsets);
+        perm::scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, cfg->E, cfg->T, cfg->K, blk_base, offs, counts);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status moe_quant_fp8_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q, float* scale,
+                               void* stream) {
+    if (!x || !q || !scale || rows < 0 || cols < 0 || ld < cols) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || ld % 8) return MOE_ERR_INVALID_ARG;
+    if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0 || cols == 0) return MOE_OK;
+    const int64_t tiles = rows * (cols / 128);
+    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 8), static_cast<int64_t>(num_sms()) * 16));
+    quant_1x128_kernel<<<grid, 256, 0, as_stream(stream)>>>(x, rows, cols, ld, q, scale);
+    return launch_status();
+}
+
+moe_status moe_quant_fp8_128x128(const float* w, int64_t batch, int64_t rows, int64_t cols, uint8_t* q, float* scale,
+                                 void* stream) {
+    if (!w || !q || !scale || batch < 0 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(scale)) return MOE_ERR_INVALID_ARG;
+    if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int64_t blocks = batch * (rows / 128) * (cols / 128);
+    if (blocks == 0) return MOE_OK;
+    if (blocks > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    quant_128x128_kernel<<<static_cast<unsigned>(blocks), 256, 0, as_stream(stream)>>>(w, rows, cols, q, scale);
+    return launch_status();
+}
+
+moe_status moe_pack_w13(const uint8_t* q1, const float* s1, const uint8_t* q3, const float* s3, int64_t batch,
+                        int64_t I, int64_t d, uint8_t* q13, float* s13, void* stream) {
+    if (!q1 || !s1 || !q3 || !s3 || !q13 || !s13 || batch < 0 || I < 0 || d < 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(q1) || !aligned16(q3) || !aligned16(q13)) return MOE_ERR_INVALID_ARG;
+    if (I % 128 || d % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (batch == 0 || I == 0 || d == 0) return MOE_OK;
+    cudaStream_t st = as_stream(stream);
+    const int64_t rows = batch * 2 * I;
+    pack_w13_kernel<<<static_cast<unsigned>(ceil_div(rows * 32, 256)), 256, 0, st>>>(q1, q3, batch, I, d, q13);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    const int64_t ns = batch * 2 * (I / 128) * (d / 128);
+    pack_w13_scale_kernel<<<static_cast<unsigned>(ceil_div(ns, 256)), 256, 0, st>>>(s1, s3, batch, I / 128, d / 128, s13);
+    return launch_status();
+}
+
+moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, const uint8_t* xq, const float* xs,
+                       int32_t* offsets, int32_t* counts, int32_t* sorted_token, int32_t* row_of, uint8_t* xq_perm,
+                       float* xs_perm, void* workspace, size_t workspace_bytes, void* stream) {
+    const moe_status cs = check_config(cfg);
+    if (cs != MOE_OK) return cs;
+    if (!topk_idx || !xq || !xs || !offsets || !sorted_token || !row_of || !xq_perm || !xs_perm)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(xq_perm) || !aligned16(topk_idx)) return MOE_ERR_INVALID_ARG;
+    const WsLayout wl = ws_layout(cfg);
+    if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* blk_counts = reinterpret_cast<int32_t*>(ws + wl.blk_counts);
+    int32_t* blk_base = reinterpret_cast<int32_t*>(ws + wl.blk_base);
+    const int nblk = static_cast<int>(ceil_div(cfg->T, perm::kTokPerBlk));
+    const int64_t npairs = static_cast<int64_t>(cfg->T) * cfg->K;
+    const size_t hsm = static_cast<size_t>(perm::kWarps) * cfg->E * sizeof(int);
+    perm::hist_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E, blk_counts);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    perm::scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, cfg->E, cfg->T, cfg->K, blk_base, offsets, counts);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    perm::scatter_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E, blk_base, row_of,
+                                                               sorted_token);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    const int64_t rows = npairs + cfg->T;
+    perm::gather_kernel<<<static_cast<unsigned>(ceil_div(rows * 32, 256)), 256, 0, st>>>(
+        sorted_token, cfg->T, cfg->K, cfg->d, xq, xs, xq_perm, xs_perm);
+    return launch_status();
+}
+
+moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,
+                                const uint8_t* A, const float* sa, const uint8_t* B, const float* sb, int32_t epilogue,
+                                void* out, float* out_scale, void* stream) {
+    if (!offsets || !A || !sa || !B || !sb || !out || rows < 0 || groups < 1 || N < 0 || Kdim < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8) return MOE_ERR_INVALID_ARG;
+    if (epilogue == MOE_EPI_SWIGLU_FP8 && !out_scale) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if (groups > gemm::MAX_GROUPS || N % gemm::BN || N == 0 || Kdim % gemm::BK || Kdim == 0 || rows >= INT32_MAX)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(groups) * N >= INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    CUtensorMap ta, tb;
+    if (!make_map_u8(&ta, A, static_cast<uint64_t>(Kdim), static_cast<uint64_t>(rows), gemm::BM)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&tb, B, static_cast<uint64_t>(Kdim), static_cast<uint64_t>(groups) * N, gemm::BN))
+        return MOE_ERR_CUDA;
+    gemm::Params p{offsets, groups, rows, N, Kdim, sa, sb, out, out_scale};
+    const int64_t tiles_max = (ceil_div(rows, gemm::BM) + groups) * (N / gemm::BN);
+    cudaStream_t st = as_stream(stream);
+    if (epilogue == MOE_EPI_BF16) return launch_gemm<MOE_EPI_BF16>(ta, tb, p, tiles_max, st);
+    return launch_gemm<MOE_EPI_SWIGLU_FP8>(ta, tb, p, tiles_max, st);
+}
+
+moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const uint16_t* shared_out,
+                       const int32_t* row_of, const float* topk_gate, const uint16_t* residual, uint16_t* y,
+                       void* stream) {
+    const moe_status cs = check_config(cfg);
+    if (cs != MOE_OK) return cs;
+    if (!routed_out || !shared_out || !row_of || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(routed_out) || !aligned16(shared_out) || !aligned16(y) || (residual && !aligned16(residual)))
+        return MOE_ERR_INVALID_ARG;
+    combine_kernel<<<cfg->T, 128, 0, as_stream(stream)>>>(routed_out, shared_out, row_of, topk_gate, residual, cfg->T,
+                                                          cfg->K, cfg->d, y);
+    return launch_status();
+}
+
+moe_status moe_bias_update(int32_t E, int32_t T, int32_t K, const int32_t* counts, float gamma, float* bias,
+                           void* stream) {
+    if (!counts || !bias || E < 1 || T < 0 || K < 1) return MOE_ERR_INVALID_ARG;
+    bias_update_kernel<<<static_cast<unsigned>(ceil_div(E, 256)), 256, 0, as_stream(stream)>>>(E, T, K, counts, gamma,
+                                                                                              bias);
+    return launch_status();
+}
+
+moe_status moe_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+    selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(static_cast<uint64_t>(limit_us) * 1000ull);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    return moe_check_device_status(stream);
+}
+
+}  // extern "C"

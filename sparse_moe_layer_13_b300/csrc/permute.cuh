@@ -1,0 +1,174 @@
+// Expert histogram and token permutation by expert, without atomics.
+//
+// The routed (token, slot) pairs, taken in token order, are cut into blocks
+// of kTokPerBlk tokens; each block is split into 8 contiguous warp segments.
+//  1. hist_kernel:    per-warp histograms of each segment with
+//                     __match_any_sync (the lowest lane of each run of equal
+//                     experts adds the run length), summed to per-block counts.
+//  2. scan_kernel:    one CTA: per-expert totals, exclusive prefix sum over
+//                     experts (offsets), and each block's starting row for
+//                     each expert (offsets + counts of earlier blocks).
+//  3. scatter_kernel: recomputes the per-warp histograms, turns them into
+//                     per-warp starting rows, then assigns rows in order:
+//                     rank inside a 32-pair batch = popc(same-expert lanes
+//                     below me). Writes row_of and sorted_token.
+//  4. gather_kernel:  one warp per grouped row copies the E4M3 row and its
+//                     1x128 scales (16-byte vectors); shared-expert rows
+//                     T*K + t copy token t.
+// Result: rows ordered by (expert ascending, token ascending), the order a
+// stable sort of the pairs by expert gives.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+namespace perm {
+
+constexpr int kTokPerBlk = 256;
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ int load_pair_expert(const int32_t* idx, int64_t i, int64_t n, int E) {
+    if (i >= n) return -1;
+    int e = __ldg(idx + i);
+    if (e < 0 || e >= E) { set_status(MOE_ERR_DEVICE_CHECK); return -1; }
+    return e;
+}
+
+// hist[w][e] for warp w's segment of block `blk`.
+__device__ __forceinline__ void warp_histograms(const int32_t* idx, int64_t npairs, int K, int E,
+                                                int* hist, int64_t& seg_begin, int64_t& seg_end) {
+    const int w = threadIdx.x >> 5;
+    const int64_t blk_begin = static_cast<int64_t>(blockIdx.x) * kTokPerBlk * K;
+    const int64_t blk_end = min(blk_begin + static_cast<int64_t>(kTokPerBlk) * K, npairs);
+    const int64_t seg = (blk_end - blk_begin + kWarps - 1) / kWarps;
+    seg_begin = min(blk_begin + w * seg, blk_end);
+    seg_end = min(seg_begin + seg, blk_end);
+    int* h = hist + w * E;
+    for (int64_t b = seg_begin; b < seg_end; b += 32) {
+        const int e = load_pair_expert(idx, b + lane_id(), seg_end, E);
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (__ffs(same) - 1) == static_cast<int>(lane_id())) h[e] += __popc(same);
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32) hist_kernel(const int32_t* __restrict__ idx, int64_t npairs, int K,
+                                                           int E, int32_t* __restrict__ blk_counts) {
+    extern __shared__ int hist[];   // [kWarps][E]
+    for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    int64_t sb, se;
+    warp_histograms(idx, npairs, K, E, hist, sb, se);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) c += hist[w * E + e];
+        blk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = c;
+    }
+}
+
+// Single CTA of 1024 threads. blk_base[b][e] = offsets[e] + sum_{b' < b} blk_counts[b'][e].
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ blk_counts, int nblk, int E, int T,
+                                                    int K, int32_t* __restrict__ blk_base,
+                                                    int32_t* __restrict__ offsets, int32_t* __restrict__ counts) {
+    __shared__ int warp_sums[32];
+    const int e = threadIdx.x;
+    int run = 0;
+    if (e < E) {
+        for (int b = 0; b < nblk; ++b) {
+            const int c = blk_counts[static_cast<int64_t>(b) * E + e];
+            blk_base[static_cast<int64_t>(b) * E + e] = run;
+            run += c;
+        }
+    }
+    // exclusive scan of the totals over experts
+    const int lane = static_cast<int>(lane_id()), w = e >> 5;
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int v = warp_sums[lane];
+        int vi = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, vi, o);
+            if (lane >= o) vi += t;
+        }
+        warp_sums[lane] = vi - v;
+    }
+    __syncthreads();
+    const int off = warp_sums[w] + incl - run;
+    if (e < E) {
+        offsets[e] = off;
+        if (counts != nullptr) counts[e] = run;
+        for (int b = 0; b < nblk; ++b) blk_base[static_cast<int64_t>(b) * E + e] += off;
+    }
+    if (e == 0) {
+        offsets[E] = T * K;
+        offsets[E + 1] = T * K + T;
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32) scatter_kernel(const int32_t* __restrict__ idx, int64_t npairs, int K,
+                                                              int E, const int32_t* __restrict__ blk_base,
+                                                              int32_t* __restrict__ row_of,
+                                                              int32_t* __restrict__ sorted_token) {
+    extern __shared__ int hist[];   // [kWarps][E]
+    for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    int64_t sb, se;
+    warp_histograms(idx, npairs, K, E, hist, sb, se);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = blk_base[static_cast<int64_t>(blockIdx.x) * E + e];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const int c = hist[w * E + e];
+            hist[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    int* h = hist + (threadIdx.x >> 5) * E;
+    const uint32_t lane = lane_id();
+    for (int64_t b = sb; b < se; b += 32) {
+        const int64_t i = b + lane;
+        const int e = load_pair_expert(idx, i, se, E);
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & ((1u << lane) - 1u));
+        const int row = (e >= 0) ? h[e] + rank : 0;
+        __syncwarp();
+        if (e >= 0 && (__ffs(same) - 1) == static_cast<int>(lane)) h[e] += __popc(same);
+        __syncwarp();
+        if (e >= 0) {
+            row_of[i] = row;
+            sorted_token[row] = static_cast<int32_t>(i / K);
+        }
+    }
+}
+
+// One warp per grouped row r in [0, T*K + T).
+__global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ sorted_token, int T, int K, int d,
+                                                     const uint8_t* __restrict__ xq, const float* __restrict__ xs,
+                                                     uint8_t* __restrict__ xq_perm, float* __restrict__ xs_perm) {
+    const int64_t rows = static_cast<int64_t>(T) * K + T;
+    const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (r >= rows) return;
+    const int64_t tk = static_cast<int64_t>(T) * K;
+    int src = (r < tk) ? __ldg(sorted_token + r) : static_cast<int>(r - tk);
+    if (src < 0 || src >= T) { set_status(MOE_ERR_DEVICE_CHECK); src = 0; }
+    const uint4* s = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(src) * d);
+    uint4* dst = reinterpret_cast<uint4*>(xq_perm + r * d);
+    for (int c = lane_id(); c < d / 16; c += 32) dst[c] = __ldg(s + c);
+    const int nk = d / 128;
+    for (int c = lane_id(); c < nk; c += 32) xs_perm[r * nk + c] = __ldg(xs + static_cast<int64_t>(src) * nk + c);
+}
+
+}  // namespace perm
+}  // namespace moe

@@ -1,0 +1,100 @@
+// Fine-grained FP8 quantisation ("DeepSeek-V3的MoE架构设计革新" §2 FP8 training,
+// item 1: activations per 1x128 tile, weights per 128x128 block; E4M3 largest
+// finite value 448 per "DeepSeek-V3技术解析" §6.2).
+//   scale = fl32(amax / 448), code = E4M3_RNE_SATFINITE(fl32(v / scale)).
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// One warp per 1x128 tile: 4 bf16 values per lane (8-byte loads), amax by
+// warp shuffle, 4 E4M3 codes per lane (4-byte stores). Grid-stride over
+// tiles, so any grid size is valid.
+__global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                          int64_t cols, int64_t ld, uint8_t* __restrict__ q,
+                                                          float* __restrict__ scale) {
+    const int64_t tiles_per_row = cols / 128;
+    const int64_t ntiles = rows * tiles_per_row;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const uint32_t lane = lane_id();
+    for (int64_t t = warp; t < ntiles; t += nwarps) {
+        const int64_t r = t / tiles_per_row;
+        const int64_t c = t - r * tiles_per_row;
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(x + r * ld + c * 128) + lane);
+        const float v0 = bf16_lo(w.x), v1 = bf16_hi(w.x), v2 = bf16_lo(w.y), v3 = bf16_hi(w.y);
+        float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float s = __fdiv_rn(amax, kE4M3Max);
+        const uint32_t codes = e4m3x4(quant_ratio(v0, s), quant_ratio(v1, s), quant_ratio(v2, s), quant_ratio(v3, s));
+        reinterpret_cast<uint32_t*>(q + r * cols + c * 128)[lane] = codes;
+        if (lane == 0) scale[r * tiles_per_row + c] = s;
+    }
+}
+
+// One CTA (256 threads) per 128x128 block of one matrix.
+__global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ w, int64_t rows, int64_t cols,
+                                                            uint8_t* __restrict__ q, float* __restrict__ scale) {
+    const int64_t bc = cols / 128, br = rows / 128;
+    const int64_t blk = blockIdx.x;                      // over batch * br * bc
+    const int64_t mat = blk / (br * bc);
+    const int64_t rb = (blk / bc) % br, cb = blk % bc;
+    const float* src = w + mat * rows * cols + rb * 128 * cols + cb * 128;
+    uint8_t* dst = q + mat * rows * cols + rb * 128 * cols + cb * 128;
+    __shared__ float red[8];
+    // each thread: rows (tid/32) + 8*i, 4 columns at 4*(tid%32)
+    const int tr = threadIdx.x >> 5, tc = (threadIdx.x & 31) * 4;
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src + (tr + 8 * i) * cols + tc));
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    const float s = __fdiv_rn(amax, kE4M3Max);
+    for (int i = 0; i < 16; ++i) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src + (tr + 8 * i) * cols + tc));
+        *reinterpret_cast<uint32_t*>(dst + (tr + 8 * i) * cols + tc) =
+            e4m3x4(quant_ratio(v.x, s), quant_ratio(v.y, s), quant_ratio(v.z, s), quant_ratio(v.w, s));
+    }
+    if (threadIdx.x == 0) scale[mat * br * bc + rb * bc + cb] = s;
+}
+
+// W13 row r of matrix b, for I-block j = r / 256 and p = r % 256:
+//   p in [0,64)    -> W1 row 128j + p
+//   p in [64,128)  -> W3 row 128j + p - 64
+//   p in [128,192) -> W1 row 128j + p - 64
+//   p in [192,256) -> W3 row 128j + p - 128
+// One warp per output row, 16-byte copies.
+__global__ void __launch_bounds__(256) pack_w13_kernel(const uint8_t* __restrict__ q1, const uint8_t* __restrict__ q3,
+                                                       int64_t batch, int64_t I, int64_t d,
+                                                       uint8_t* __restrict__ q13) {
+    const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (row >= batch * 2 * I) return;
+    const int64_t b = row / (2 * I), r = row % (2 * I);
+    const int64_t j = r / 256, p = r % 256;
+    const bool up = (p >= 64 && p < 128) || p >= 192;
+    const int64_t src_row = 128 * j + (p < 128 ? (p % 64) : 64 + (p % 64));
+    const uint8_t* src = (up ? q3 : q1) + (b * I + src_row) * d;
+    uint8_t* dst = q13 + row * d;
+    for (int64_t c = lane_id() * 16; c < d; c += 32 * 16)
+        *reinterpret_cast<uint4*>(dst + c) = __ldg(reinterpret_cast<const uint4*>(src + c));
+}
+
+__global__ void pack_w13_scale_kernel(const float* __restrict__ s1, const float* __restrict__ s3, int64_t batch,
+                                      int64_t nbi, int64_t nbk, float* __restrict__ s13) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;   // over batch*2*nbi*nbk
+    if (i >= batch * 2 * nbi * nbk) return;
+    const int64_t kc = i % nbk, rb = (i / nbk) % (2 * nbi), b = i / (nbk * 2 * nbi);
+    const float* src = (rb & 1) ? s3 : s1;
+    s13[i] = src[(b * nbi + rb / 2) * nbk + kc];
+}
+
+}  // namespace moe

@@ -1,0 +1,110 @@
+"""DeepSeekMoE layer forward on one B300, chaining the C-ABI calls.
+
+《DeepSeek-V3 Technical Report》深度解读报告 §2.2-§2.4 and "DeepSeek-V3的MoE架构
+设计革新" §2 describe the layer; this module only owns device buffers and
+calls, in order: moe_route -> moe_quant_fp8_1x128 -> moe_permute ->
+moe_grouped_gemm_fp8 (gate/up + SwiGLU + requantisation) ->
+moe_grouped_gemm_fp8 (down) -> moe_combine -> moe_bias_update.
+Expert E (the last group) is the shared expert.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+from . import inputs
+from .configs import MoEConfig
+
+
+class ExpertWeights:
+    """FP8 expert weights on the device, built from the seeded generator.
+
+    q13 u8 [E+1][2I][d] (SwiGLU layout), s13 f32 [E+1][2I/128][d/128],
+    q2  u8 [E+1][d][I],                  s2  f32 [E+1][d/128][I/128].
+    """
+
+    def __init__(self, cfg: MoEConfig, device="cuda", chunk: int = 16):
+        E1, I, d = cfg.E + 1, cfg.I, cfg.d
+        self.q13 = torch.empty(E1, 2 * I, d, dtype=torch.uint8, device=device)
+        self.s13 = torch.empty(E1, 2 * I // 128, d // 128, dtype=torch.float32, device=device)
+        self.q2 = torch.empty(E1, d, I, dtype=torch.uint8, device=device)
+        self.s2 = torch.empty(E1, d // 128, I // 128, dtype=torch.float32, device=device)
+        for e0 in range(0, E1, chunk):
+            e1 = min(E1, e0 + chunk)
+            ws = [inputs.gen_expert(cfg, e, device) for e in range(e0, e1)]
+            w1 = torch.stack([w[0] for w in ws])
+            w3 = torch.stack([w[1] for w in ws])
+            w2 = torch.stack([w[2] for w in ws])
+            del ws
+            q1, s1 = B.quant_128x128(w1)
+            q3, s3 = B.quant_128x128(w3)
+            B.pack_w13(q1, s1, q3, s3, self.q13[e0:e1], self.s13[e0:e1])
+            B.quant_128x128(w2, self.q2[e0:e1], self.s2[e0:e1])
+            del w1, w3, w2, q1, q3
+
+
+class MoELayer:
+    """One layer instance: router weight, selection bias, expert weights, buffers."""
+
+    def __init__(self, cfg: MoEConfig, device="cuda", weights: ExpertWeights | None = None,
+                 logit_offset: torch.Tensor | None = None):
+        self.cfg = cfg
+        self.device = device
+        self.Wr = inputs.gen_router(cfg, device)
+        self.bias = inputs.gen_bias(cfg, device)
+        self.logit_offset = logit_offset
+        self.w = ExpertWeights(cfg, device) if weights is None else weights
+        T, K, E, d, I = cfg.T, cfg.K, cfg.E, cfg.d, cfg.I
+        R = cfg.rows
+        z = lambda *s, dt: torch.empty(*s, dtype=dt, device=device)  # noqa: E731
+        self.ws = z(B.workspace_size(cfg), dt=torch.uint8)
+        self.idx = z(T, K, dt=torch.int32)
+        self.gate = z(T, K, dt=torch.float32)
+        self.counts = z(E, dt=torch.int32)
+        self.xq = z(T, d, dt=torch.uint8)
+        self.xs = z(T, d // 128, dt=torch.float32)
+        self.perm = {
+            "offsets": z(E + 2, dt=torch.int32), "counts": None,
+            "sorted_token": z(T * K, dt=torch.int32), "row_of": z(T, K, dt=torch.int32),
+            "xq_perm": z(R, d, dt=torch.uint8), "xs_perm": z(R, d // 128, dt=torch.float32),
+        }
+        self.hq = z(R, I, dt=torch.uint8)
+        self.hs = z(R, I // 128, dt=torch.float32)
+        self.out = z(R, d, dt=torch.bfloat16)
+        self.y = z(T, d, dt=torch.bfloat16)
+
+    def forward(self, x: torch.Tensor, residual: bool = False, update_bias: bool = True,
+                gamma: float | None = None, counts_hook=None, events=None) -> torch.Tensor:
+        """One layer forward on the current stream.
+
+        counts_hook(counts) runs before the bias update (e.g. an all-reduce of
+        the expert load across data-parallel ranks); events, if given, is a
+        dict of name -> (start, end) torch.cuda.Event pairs recorded around
+        the two grouped GEMMs ("gemm1", "gemm2").
+        """
+        c = self.cfg
+        ev = events or {}
+        B.route(c, x, self.Wr, self.bias, self.logit_offset, self.ws, self.idx, self.gate, self.counts)
+        B.quant_1x128(x, self.xq, self.xs)
+        B.permute(c, self.idx, self.xq, self.xs, self.ws, self.perm)
+        if "gemm1" in ev:
+            ev["gemm1"][0].record()
+        B.grouped_gemm_fp8(self.perm["offsets"], self.perm["xq_perm"], self.perm["xs_perm"], self.w.q13, self.w.s13,
+                           B.MOE_EPI_SWIGLU_FP8, self.hq, self.hs)
+        if "gemm1" in ev:
+            ev["gemm1"][1].record()
+        if "gemm2" in ev:
+            ev["gemm2"][0].record()
+        B.grouped_gemm_fp8(self.perm["offsets"], self.hq, self.hs, self.w.q2, self.w.s2, B.MOE_EPI_BF16, self.out)
+        if "gemm2" in ev:
+            ev["gemm2"][1].record()
+        TK = c.T * c.K
+        B.combine(c, self.out[:TK], self.out[TK:], self.perm["row_of"], self.gate, x if residual else None, self.y)
+        if update_bias:
+            if counts_hook is not None:
+                counts_hook(self.counts)
+            B.bias_update(c.E, c.T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
+        return self.y
+
+    # launches per forward: route 2 (+2 with counts), quant 1, permute 4, GEMMs 2, combine 1, bias 1
+    LAUNCHES_PER_FORWARD = 13

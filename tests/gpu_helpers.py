@@ -1,0 +1,79 @@
+"""Shared pieces of the GPU parity tests: device setup, seeded inputs for both
+sides, oracle construction, and the comparison rules.
+
+Tolerances (floating point): router gates within 1e-5 absolute; layer output
+relative L2 <= 5e-3 and max |diff| <= 2e-2 * RMS of the reference. Integer and
+byte results (E4M3 codes, scales, histograms, permutation) are compared
+bit for bit. Tokens whose routing hinges on a margin below 1e-6 (the oracle
+reports them) are excluded from routing and layer comparisons.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+gpu = pytest.mark.gpu
+
+GATE_ATOL = 1e-5
+Y_REL_L2 = 5e-3
+Y_MAX_RMS = 2e-2
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.detach().cpu().numpy()
+
+
+def y_metrics(got: np.ndarray, want: np.ndarray):
+    diff = got.astype(np.float64) - want.astype(np.float64)
+    rel = np.linalg.norm(diff) / max(np.linalg.norm(want), 1e-300)
+    rms = np.sqrt(np.mean(want.astype(np.float64) ** 2))
+    return rel, np.abs(diff).max() / max(rms, 1e-300)
+
+
+def assert_y_close(got, want):
+    rel, mx = y_metrics(got, want)
+    assert rel <= Y_REL_L2, f"rel-L2 {rel:.3e}"
+    assert mx <= Y_MAX_RMS, f"max-abs/RMS {mx:.3e}"
+    return rel, mx
+
+
+def oracle_experts(cfg, experts, device="cuda"):
+    """Quantised oracle experts for `experts`, built in parallel CPU workers.
+
+    The fp32 weights come from the same seeded generator (on `device`) that
+    fed the CUDA path; the workers run only the oracle's quantiser.
+    """
+    from oracle.parallel import quantize_experts
+    from sparse_moe_layer_13_b300.inputs import gen_expert
+    jobs = [(e, *(to_np(w) for w in gen_expert(cfg, e, device))) for e in sorted(set(int(e) for e in experts))]
+    return quantize_experts(jobs)
+
+
+def check_routing(cfg, idx_gpu, gate_gpu, ref_idx, ref_gate, info):
+    """Bit-exact expert choice and order, gates within GATE_ATOL, on non-tie tokens."""
+    from oracle.route import near_tie
+    tie = near_tie(info)
+    ok = ~tie
+    gi = np.asarray(idx_gpu)
+    gg = np.asarray(gate_gpu)
+    assert np.array_equal(np.sort(gi[ok], 1), np.sort(ref_idx[ok], 1)), "chosen expert sets differ"
+    strict = ok & (info["order_gap"] > 1e-6)
+    assert np.array_equal(gi[strict], ref_idx[strict]), "order of chosen experts differs"
+    o1 = np.argsort(gi[ok], 1)
+    o2 = np.argsort(ref_idx[ok], 1)
+    g1 = np.take_along_axis(gg[ok], o1, 1)
+    g2 = np.take_along_axis(ref_gate[ok], o2, 1)
+    err = np.abs(g1 - g2).max() if g1.size else 0.0
+    assert err <= GATE_ATOL, f"gate error {err:.3e}"
+    return tie, err

@@ -1,0 +1,83 @@
+"""The C-ABI library loads without a GPU, exports every symbol its header
+declares, and rejects bad arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_b300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from sparse_moe_layer_13_b300 import binding
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_six_calls():
+    names = declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_quant_fp8_1x128", "moe_grouped_gemm_fp8", "moe_combine",
+              "moe_bias_update"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from sparse_moe_layer_13_b300 import binding
+    for code, name in binding.STATUS.items():
+        assert lib.moe_status_string(code).decode().startswith(name)
+    assert lib.moe_status_string(99).decode() == "MOE_ERR_UNKNOWN"
+
+
+def test_workspace_size_and_config_checks(lib):
+    from sparse_moe_layer_13_b300 import binding
+    from sparse_moe_layer_13_b300.configs import CONFIGS, MoEConfig
+    for cfg in CONFIGS.values():
+        assert binding.workspace_size(cfg) >= cfg.T * cfg.E * 4
+    bad = [
+        MoEConfig("b", T=8, d=200, E=16, I=128, K=2, G=4, M=2, gk=2, seed=0),    # d % 128
+        MoEConfig("b", T=8, d=128, E=20, I=128, K=2, G=4, M=2, gk=2, seed=0),    # E % 16
+        MoEConfig("b", T=8, d=128, E=16, I=128, K=2, G=4, M=5, gk=2, seed=0),    # M > G
+        MoEConfig("b", T=8, d=128, E=16, I=128, K=9, G=4, M=2, gk=2, seed=0),    # K > M*E/G
+        MoEConfig("b", T=8, d=128, E=16, I=128, K=2, G=4, M=2, gk=5, seed=0),    # gk > E/G
+        MoEConfig("b", T=0, d=128, E=16, I=128, K=2, G=4, M=2, gk=2, seed=0),    # T < 1
+    ]
+    for cfg in bad:
+        assert binding.workspace_size(cfg) == 0
+
+
+def test_host_side_errors_return_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)          # aligned, never dereferenced: every call below fails its host checks
+    odd = P(0x10001)
+    assert lib.moe_quant_fp8_1x128(None, 4, 128, 128, fake, fake, None) == 1
+    assert lib.moe_quant_fp8_1x128(fake, 4, 100, 128, fake, fake, None) == 2
+    assert lib.moe_quant_fp8_1x128(odd, 4, 128, 128, fake, fake, None) == 1
+    assert lib.moe_quant_fp8_128x128(fake, 1, 100, 128, fake, fake, None) == 2
+    assert lib.moe_grouped_gemm_fp8(4, fake, 100, 200, 256, fake, fake, fake, fake, 0, fake, None, None) == 2
+    assert lib.moe_grouped_gemm_fp8(4, fake, 100, 256, 200, fake, fake, fake, fake, 0, fake, None, None) == 2
+    assert lib.moe_grouped_gemm_fp8(4, fake, 100, 256, 256, fake, fake, fake, fake, 7, fake, None, None) == 1
+    assert lib.moe_grouped_gemm_fp8(4, fake, 100, 256, 256, fake, fake, fake, fake, 1, fake, None, None) == 1
+    assert lib.moe_grouped_gemm_fp8(2000, fake, 100, 256, 256, fake, fake, fake, fake, 0, fake, None, None) == 2
+    assert lib.moe_bias_update(0, 4, 2, fake, ctypes.c_float(0.1), fake, None) == 1
+    assert lib.moe_combine(None, fake, fake, fake, fake, None, fake, None) == 1
+    from sparse_moe_layer_13_b300 import binding
+    from sparse_moe_layer_13_b300.configs import TINY
+    c = binding.config_c(TINY)
+    # workspace too small
+    assert lib.moe_permute(ctypes.byref(c), fake, fake, fake, fake, None, fake, fake, fake, fake, fake, 16, None) == 3
+    assert lib.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, fake, None, None, 0, None) == 3

@@ -1,0 +1,129 @@
+"""GPU parity: grouped FP8 GEMM (tcgen05) against the oracle's scaled FP8
+contraction, on ragged groups (empty, single-row, tile-straddling), both
+epilogues, and a corrupt offsets table."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import gpu, require_gpu, to_np
+from oracle import e4m3
+from oracle.ffn import gemm_fp8, round_bf16, silu
+from oracle.quant import dequant_1x128, quant_1x128
+
+
+def _codes(rng, shape):
+    c = rng.integers(0, 256, shape, dtype=np.uint8)
+    c[(c & 0x7F) == 0x7F] -= 1            # no NaN codes
+    return c
+
+
+def _problem(sizes, N, K, seed, trailing=0):
+    rng = np.random.default_rng(seed)
+    G = len(sizes)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    rows = int(offsets[-1]) + trailing
+    A = _codes(rng, (rows, K))
+    sa = rng.uniform(0.5, 2.0, (rows, K // 128)).astype(np.float32) / 448
+    B = _codes(rng, (G, N, K))
+    sb = rng.uniform(0.5, 2.0, (G, N // 128, K // 128)).astype(np.float32) / 448
+    return offsets, A, sa, B, sb
+
+
+def _cuda(*arrs):
+    return [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in arrs]
+
+
+SIZES = [
+    [0, 1, 127, 128, 129, 300, 0, 513],
+    [256],
+    [5, 0, 0, 0, 1000],
+]
+
+
+@gpu
+@pytest.mark.parametrize("case", range(len(SIZES)))
+@pytest.mark.parametrize("N,K", [(256, 128), (512, 384), (768, 1024)])
+def test_gemm_bf16_epilogue(case, N, K):
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding
+    offsets, A, sa, B, sb = _problem(SIZES[case], N, K, seed=case * 100 + N + K, trailing=70)
+    o_d, A_d, sa_d, B_d, sb_d = _cuda(offsets, A, sa, B, sb)
+    out = torch.full((A.shape[0], N), -7.0, dtype=torch.bfloat16, device="cuda")
+    binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, binding.MOE_EPI_BF16, out)
+    binding.check_device_status()
+    got = to_np(out).astype(np.float64)
+    absA, absB = A & 0x7F, B & 0x7F
+    for g in range(len(offsets) - 1):
+        r0, r1 = offsets[g], offsets[g + 1]
+        if r1 == r0:
+            continue
+        exact = gemm_fp8(A[r0:r1], sa[r0:r1], B[g], sb[g])
+        mag = gemm_fp8(absA[r0:r1], sa[r0:r1], absB[g], sb[g])
+        err = np.abs(got[r0:r1] - exact)
+        assert np.all(err <= 2.0 ** -8 * np.abs(exact) + 1e-5 * mag + 1e-30), f"group {g}"
+        assert np.mean(got[r0:r1] == round_bf16(exact)) > 0.99
+    assert np.all(got[offsets[-1]:] == -7.0)       # rows outside every group untouched
+
+
+@gpu
+@pytest.mark.parametrize("case", range(len(SIZES)))
+@pytest.mark.parametrize("I,K", [(128, 256), (384, 512)])
+def test_gemm_swiglu_epilogue(case, I, K):
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding
+    rng = np.random.default_rng(case + I)
+    sizes = SIZES[case]
+    G = len(sizes)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    rows = int(offsets[-1]) + 3
+    # realistic magnitudes: quantise N(0,1) activations and N(0,1/K) weights with the oracle
+    xq, xs = quant_1x128(rng.standard_normal((rows, K)).astype(np.float32))
+    from oracle.quant import quant_128x128
+    W1 = [quant_128x128((rng.standard_normal((I, K)) / np.sqrt(K)).astype(np.float32)) for _ in range(G)]
+    W3 = [quant_128x128((rng.standard_normal((I, K)) / np.sqrt(K)).astype(np.float32)) for _ in range(G)]
+    q1 = np.stack([w[0] for w in W1]); s1 = np.stack([w[1] for w in W1])
+    q3 = np.stack([w[0] for w in W3]); s3 = np.stack([w[1] for w in W3])
+    q1_d, s1_d, q3_d, s3_d, o_d, xq_d, xs_d = _cuda(q1, s1, q3, s3, offsets, xq, xs)
+    q13, s13 = binding.pack_w13(q1_d, s1_d, q3_d, s3_d)
+    hq = torch.full((rows, I), 0x55, dtype=torch.uint8, device="cuda")
+    hs = torch.full((rows, I // 128), -1.0, dtype=torch.float32, device="cuda")
+    binding.grouped_gemm_fp8(o_d, xq_d, xs_d, q13, s13, binding.MOE_EPI_SWIGLU_FP8, hq, hs)
+    binding.check_device_status()
+    ghq, ghs = to_np(hq), to_np(hs)
+    for g in range(G):
+        r0, r1 = offsets[g], offsets[g + 1]
+        if r1 == r0:
+            continue
+        gate = gemm_fp8(xq[r0:r1], xs[r0:r1], q1[g], s1[g])
+        up = gemm_fp8(xq[r0:r1], xs[r0:r1], q3[g], s3[g])
+        h = (silu(gate) * up).astype(np.float32)
+        rq, rs = quant_1x128(h)
+        assert np.allclose(ghs[r0:r1], rs, rtol=1e-5, atol=0), f"scales of group {g}"
+        assert np.mean(ghq[r0:r1] == rq) > 0.99
+        dg = dequant_1x128(ghq[r0:r1], ghs[r0:r1])
+        dr = dequant_1x128(rq, rs)
+        tol = 0.13 * np.abs(dr) + 2.0 ** -9 * np.repeat(rs, 128, axis=1) * 1.01 + 1e-30
+        assert np.all(np.abs(dg - dr) <= tol)
+    assert np.all(ghq[offsets[-1]:] == 0x55) and np.all(ghs[offsets[-1]:] == -1.0)
+
+
+@gpu
+def test_gemm_reports_corrupt_offsets():
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding
+    offsets, A, sa, B, sb = _problem([10, 20, 30], 256, 128, seed=1)
+    bad = offsets.copy()
+    bad[2] = 5                      # not monotone
+    o_d, A_d, sa_d, B_d, sb_d = _cuda(bad, A, sa, B, sb)
+    out = torch.full((A.shape[0], 256), 3.0, dtype=torch.bfloat16, device="cuda")
+    binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, binding.MOE_EPI_BF16, out)
+    with pytest.raises(binding.MoeError) as e:
+        binding.check_device_status()
+    assert e.value.code == 6
+    assert torch.all(out == 3.0)    # nothing written
+    bad = offsets.copy()
+    bad[-1] = A.shape[0] + 1        # past the last row
+    o_d = _cuda(bad)[0]
+    binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, binding.MOE_EPI_BF16, out)
+    with pytest.raises(binding.MoeError):
+        binding.check_device_status()

@@ -1,0 +1,86 @@
+"""GPU parity: the whole layer forward (route -> quant -> permute -> GEMM1
+with SwiGLU -> GEMM2 -> combine -> bias update) against the FP64 oracle on
+the workload shapes; at full width the oracle evaluates a seeded sample of
+tokens."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_y_close, check_routing, gpu, oracle_experts, require_gpu, to_np
+from oracle.layer import Layer, bias_update
+from oracle.permute import histogram
+from oracle.route import near_tie, route as oracle_route
+from sparse_moe_layer_13_b300.configs import CONFIGS
+
+
+def _layer_case(cfg, n_sample=None, residual=False, seed=0):
+    from sparse_moe_layer_13_b300 import binding, inputs
+    from sparse_moe_layer_13_b300.layer import MoELayer
+    layer = MoELayer(cfg, "cuda")
+    x = inputs.gen_x(cfg, "cuda")
+    b0 = to_np(layer.bias).copy()
+    y = to_np(layer.forward(x, residual=residual, update_bias=True))
+    binding.check_device_status()
+    xn, Wr = to_np(x), to_np(layer.Wr)
+    ref_idx, ref_gate, info = oracle_route(xn, Wr, b0, cfg.G, cfg.M, cfg.K, cfg.gk)
+    check_routing(cfg, to_np(layer.idx), to_np(layer.gate), ref_idx, ref_gate, info)
+    tie = near_tie(info)
+    if n_sample is None:
+        tokens = np.arange(cfg.T)
+    else:
+        rng = np.random.default_rng(seed)
+        tokens = np.sort(rng.choice(np.nonzero(~tie)[0], n_sample, replace=False))
+    needed = set(ref_idx[tokens].ravel().tolist()) | {cfg.E}
+    ex = oracle_experts(cfg, needed)
+    ref = Layer(cfg, Wr, b0, None, experts=ex).forward(xn, tokens=tokens, idx=ref_idx, gate=ref_gate,
+                                                       residual=residual)
+    keep = ~tie[tokens]
+    rel, mx = assert_y_close(y[tokens][keep], ref["y"][keep])
+    # end-of-step bias update, bit-exact, from the oracle's own load
+    if not tie.any():
+        want_b = bias_update(b0, histogram(ref_idx, cfg.E), cfg.T, cfg.K, cfg.gamma)
+        assert np.array_equal(to_np(layer.bias), want_b)
+    return rel, mx, layer
+
+
+@gpu
+def test_layer_tiny():
+    require_gpu()
+    _layer_case(CONFIGS["tiny"])
+
+
+@gpu
+def test_layer_tiny_residual():
+    require_gpu()
+    _layer_case(CONFIGS["tiny"], residual=True)
+
+
+@gpu
+def test_layer_mid():
+    require_gpu()
+    _layer_case(CONFIGS["mid"])
+
+
+@gpu
+def test_layer_decode_sampled():
+    require_gpu()
+    _layer_case(CONFIGS["decode"], n_sample=6, seed=1)
+
+
+@gpu
+def test_layer_full_width_prefill_sampled():
+    require_gpu()
+    _layer_case(CONFIGS["full"], n_sample=6, seed=2)
+
+
+@gpu
+def test_layer_is_deterministic():
+    require_gpu()
+    from sparse_moe_layer_13_b300 import inputs
+    from sparse_moe_layer_13_b300.layer import MoELayer
+    cfg = CONFIGS["mid"]
+    layer = MoELayer(cfg, "cuda")
+    x = inputs.gen_x(cfg, "cuda")
+    y1 = layer.forward(x, update_bias=False).clone()
+    y2 = layer.forward(x, update_bias=False).clone()
+    assert torch.equal(y1, y2)

@@ -62,3 +62,12 @@ def test_matches_torch_cast_in_range():
 def test_saturates_instead_of_nan():
     v = np.array([448.0, 464.0, 480.0, 1e30, np.inf, -np.inf], dtype=np.float32)
     assert list(e4m3.encode(v)) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+
+
+def test_two_encoders_agree():
+    rng = np.random.default_rng(9)
+    v = np.concatenate([rng.standard_normal(300_000).astype(np.float32) * 100,
+                        np.ldexp(rng.uniform(-1, 1, 100_000), rng.integers(-16, 10, 100_000)).astype(np.float32),
+                        e4m3.DECODE_TABLE[:0x7F].astype(np.float32),
+                        ((e4m3.DECODE_TABLE[:0x7E] + e4m3.DECODE_TABLE[1:0x7F]) / 2).astype(np.float32)])
+    assert np.array_equal(e4m3.encode(v), e4m3.encode_by_search(v))
