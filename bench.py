@@ -108,8 +108,8 @@ def run_ours(args):
     import torch.distributed as dist
 
     import __graft_entry__
-    from sparse_moe_layer_13_b300 import binding, inputs
-    from sparse_moe_layer_13_b300.configs import CONFIGS
+    from sparse_moe_layer_13_b300 import binding, dp, inputs
+    from sparse_moe_layer_13_b300.configs import CONFIGS, PROFILE_CONFIGS
     from sparse_moe_layer_13_b300.layer import MoELayer
 
     ws, rank, local = dist_env()
@@ -121,13 +121,13 @@ def run_ours(args):
         __graft_entry__.build()
     if ws > 1:
         dist.barrier()
-    cfg = CONFIGS[args.config]
+    cfg = {**CONFIGS, **PROFILE_CONFIGS}[args.config]
     layer = MoELayer(cfg, dev)
     # each rank its own tokens: a different x batch per rank
     x = inputs.gen_x(cfg, dev, step=rank)
-    hook = (lambda c: dist.all_reduce(c)) if ws > 1 else None
-    # bias update counts the whole data-parallel batch: scale T by ranks
-    T_all = cfg.T * ws
+    hook = dp.allreduce_load if ws > 1 else None
+    # the bias update judges the load of the whole data-parallel batch
+    T_all = dp.global_tokens(cfg.T)
 
     def _step(events=None):
         y = layer.forward(x, update_bias=False, events=events)
@@ -200,7 +200,8 @@ def run_ours(args):
         "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic (seeded N(0,1) x, N(0,1/d) weights, random init)",
         "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E}+1 I={cfg.I} K={cfg.K} G={cfg.G} M={cfg.M}",
                    "tokens_per_gpu": cfg.T, "global_tokens": tokens, "parallelism": f"dp{ws}",
-                   "l2": "inputs exceed L2 (x 235 MB, FP8 weights 11.3 GB per step)"},
+                   "l2": (f"inputs exceed L2: x {cfg.T * cfg.d * 2 / 1e6:.0f} MB and FP8 expert weights "
+                          f"{(cfg.E + 1) * 3 * cfg.d * cfg.I / 1e9:.2f} GB read every step, no flush")},
         "layer_tflops": round(cfg.flops() * ws / (ms * 1e-3) / 1e12, 1),
         "gemm": {"gate_up_swiglu_ms": round(g1, 4), "gate_up_tflops": round(g1_tflops, 1),
                  "down_ms": round(g2, 4), "down_tflops": round(g2_tflops, 1),
@@ -252,8 +253,11 @@ def cpu_baseline(cfg, n_tokens: int, steps: int):
     for s in samples:
         layer.forward(x[s])
     dt = time.perf_counter() - t
-    from threadpoolctl import threadpool_info
-    blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    try:
+        from threadpoolctl import threadpool_info
+        blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except ImportError:      # OpenBLAS uses every host core unless told otherwise
+        blas = int(os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or os.cpu_count())
     return {"value": round(n_tokens * steps / dt, 4), "unit": UNIT, "cores": blas, "kind": "oracle",
             "sample": f"{n_tokens * steps} tokens of the {cfg.name} batch (whole layer per token: route, "
                       f"quantise, {cfg.K}+1 expert FFNs in FP64, combine); weight quantisation untimed",

@@ -71,7 +71,9 @@ typedef enum moe_epilogue {
     /* SwiGLU + 1x128 requantisation. B holds gate (W1) and up (W3) rows
      * interleaved as moe_pack_w13 writes them; out: E4M3 [rows][N/2],
      * out_scale: f32 [rows][N/256]. */
-    MOE_EPI_SWIGLU_FP8 = 1
+    MOE_EPI_SWIGLU_FP8 = 1,
+    /* out: f32 [rows][N]. */
+    MOE_EPI_F32 = 2
 } moe_epilogue;
 
 /* Human-readable name of a status. Never NULL. */
@@ -188,11 +190,12 @@ moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t 
  * §2.2): y[t] = shared_out[t] + sum_k topk_gate[t][k] * routed_out[row_of[t][k]]
  * (+ residual[t] if residual != NULL), accumulated in FP32 in that order,
  * rounded to bf16.
- *   routed_out device bf16 [T*K][d]; shared_out device bf16 [T][d]
+ *   routed_out device f32 [T*K][d]; shared_out device f32 [T][d]
+ *   (the expert outputs of moe_grouped_gemm_fp8 with MOE_EPI_F32)
  *   row_of     device i32 [T][K] (values in [0, T*K), else MOE_ERR_DEVICE_CHECK)
  *   topk_gate  device f32 [T][K]; residual device bf16 [T][d] or NULL
  *   y          device bf16 [T][d] out */
-moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const uint16_t* shared_out,
+moe_status moe_combine(const moe_config* cfg, const float* routed_out, const float* shared_out,
                        const int32_t* row_of, const float* topk_gate, const uint16_t* residual,
                        uint16_t* y, void* stream);
 

@@ -15,19 +15,24 @@ from __future__ import annotations
 import numpy as np
 
 from . import route as _route
-from .ffn import QuantExpert, expert_forward, round_bf16
+from .ffn import QuantExpert, expert_forward
 from .permute import histogram
 from .quant import quant_1x128
 
 
 def combine(shared_out, routed_out, gate, residual=None) -> np.ndarray:
-    """shared_out [T][d], routed_out [T][K][d], gate [T][K] -> bf16-valued float64 [T][d]."""
+    """shared_out [T][d], routed_out [T][K][d], gate [T][K] -> float64 [T][d].
+
+    The result is left unrounded: it is the exact layer value for these
+    expert outputs, against which a bf16 result is judged (its own rounding
+    to bf16 is part of the error it is charged with).
+    """
     y = np.asarray(shared_out, np.float64).copy()
     for k in range(routed_out.shape[1]):
         y += np.asarray(gate, np.float64)[:, k][:, None] * routed_out[:, k, :]
     if residual is not None:
         y += np.asarray(residual, np.float64)
-    return round_bf16(y)
+    return y
 
 
 def bias_update(bias, counts, T: int, K: int, gamma: float) -> np.ndarray:

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
 
 MOE_EPI_BF16 = 0
 MOE_EPI_SWIGLU_FP8 = 1
+MOE_EPI_F32 = 2
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE",
@@ -204,6 +205,8 @@ def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out
     _need(sb, torch.float32, "sb", (groups, N // 128, Kdim // 128))
     if epilogue == MOE_EPI_BF16:
         out = torch.empty(rows, N, dtype=torch.bfloat16, device=A.device) if out is None else out
+    elif epilogue == MOE_EPI_F32:
+        out = torch.empty(rows, N, dtype=torch.float32, device=A.device) if out is None else out
     else:
         out = torch.empty(rows, N // 2, dtype=torch.uint8, device=A.device) if out is None else out
         out_scale = (torch.empty(rows, N // 256, dtype=torch.float32, device=A.device)
@@ -214,6 +217,11 @@ def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out
 
 
 def combine(cfg, routed_out, shared_out, row_of, gate, residual=None, y=None):
+    """routed_out f32 [T*K][d], shared_out f32 [T][d] -> y bf16 [T][d]."""
+    _need(routed_out, torch.float32, "routed_out", (cfg.T * cfg.K, cfg.d))
+    _need(shared_out, torch.float32, "shared_out", (cfg.T, cfg.d))
+    _need(row_of, torch.int32, "row_of", (cfg.T, cfg.K))
+    _need(gate, torch.float32, "topk_gate", (cfg.T, cfg.K))
     y = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=row_of.device) if y is None else y
     c = config_c(cfg)
     _call("moe_combine", ctypes.byref(c), _ptr(routed_out), _ptr(shared_out), _ptr(row_of), _ptr(gate),

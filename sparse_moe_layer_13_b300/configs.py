@@ -66,3 +66,9 @@ SKEW = MoEConfig("skew", T=65536, d=7168, E=256, I=2048, K=8, G=8, M=4, gk=2, se
                  skew_steps=50, gamma=1e-3, zipf_s=1.1)
 
 CONFIGS = {c.name: c for c in (TINY, MID, FULL, DECODE, SKEW)}
+
+# Full-width layer shapes (d, I, K, 56 K-chunks per tile) with only 32 routed
+# experts and 4096 tokens: the same per-tile GEMM behaviour as the full-width
+# prefill in about 3 GB of device memory, for kernel profiles.
+FULLWIDTH_SMALL = MoEConfig("fullwidth_small", T=4096, d=7168, E=32, I=2048, K=8, G=8, M=4, gk=2, seed=5)
+PROFILE_CONFIGS = {FULLWIDTH_SMALL.name: FULLWIDTH_SMALL}

@@ -227,6 +227,35 @@ __device__ __forceinline__ void tmem_reg_fence(uint32_t (&r)[32]) {
         : "memory");
 }
 
+// acc[0..1] += f * (v0, v1) with one packed FP32 FMA (fma.rn.f32x2).
+__device__ __forceinline__ void ffma2(float& a0, float& a1, uint32_t v0, uint32_t v1, float f) {
+    asm("{\n"
+        ".reg .b64 a, v, s;\n"
+        "mov.b64 a, {%0, %1};\n"
+        "mov.b64 v, {%2, %3};\n"
+        "mov.b64 s, {%4, %4};\n"
+        "fma.rn.f32x2 a, v, s, a;\n"
+        "mov.b64 {%0, %1}, a;\n"
+        "}\n"
+        : "+f"(a0), "+f"(a1)
+        : "r"(v0), "r"(v1), "f"(f));
+}
+
+// 32-byte vector store (sm_100+).
+__device__ __forceinline__ void st_v8_b32(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                          uint32_t f, uint32_t g, uint32_t h) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h) : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy (completes per thread, in groups).
+__device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

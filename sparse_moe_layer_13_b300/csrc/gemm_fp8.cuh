@@ -61,6 +61,8 @@ struct Smem {
     int row_start[MAX_GROUPS + 1];    // offsets[g]
     int mtile_prefix[MAX_GROUPS + 1]; // exclusive prefix of ceil(m_g / BM)
     float amax_x[2][8][32];
+    float ring_sa[4][256];            // per-thread activation scale of chunks kc .. kc+3
+    float ring_sb[4][8][2];           // per-warp weight scales (two 128-column blocks)
 };
 
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Smem);
@@ -214,6 +216,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         const int q = warp & 3;              // TMEM lane quadrant this warp may access
         const int half = ew >> 2;            // column half of the 256-wide tile
         const int rit = q * 32 + static_cast<int>(lane);
+        const int et = ew * 32 + static_cast<int>(lane);
         const int nbn = p.N / 128;
         uint32_t it = 0, tcount = 0;
         bool ok = true;
@@ -224,47 +227,83 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             const bool valid = rit < m_valid;
             const int64_t row = static_cast<int64_t>(s.row_start[g]) + mt * BM + rit;
             const float* sa_row = p.sa + (valid ? row : 0) * nkc;
-            // weight scale rows: SwiGLU -> gate block 2*nt, up block 2*nt+1; bf16 -> block 2*nt+half
+            // weight scale rows: SwiGLU -> gate block 2*nt, up block 2*nt+1; otherwise block 2*nt+half
             const float* sb0 = p.sb + (static_cast<int64_t>(g) * nbn + 2 * nt + (EPI == MOE_EPI_SWIGLU_FP8 ? 0 : half)) * nkc;
-            const float* sb1 = p.sb + (static_cast<int64_t>(g) * nbn + 2 * nt + 1) * nkc;
+            const float* sb1 = (EPI == MOE_EPI_SWIGLU_FP8) ? sb0 + nkc : sb0;
+            // scales of chunk kc are fetched asynchronously three chunks ahead into a 4-slot ring
+            auto prefetch = [&](int kc) {
+                if (kc < nkc) {
+                    const int slot = kc & 3;
+                    cp_async_4(&s.ring_sa[slot][et], sa_row + kc);
+                    if (lane == 0) {
+                        cp_async_4(&s.ring_sb[slot][ew][0], sb0 + kc);
+                        cp_async_4(&s.ring_sb[slot][ew][1], sb1 + kc);
+                    }
+                }
+                cp_async_commit();
+            };
+            prefetch(0);
+            prefetch(1);
+            prefetch(2);
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
             for (int kc = 0; kc < nkc; ++kc, ++it) {
                 const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-                const float sav = valid ? __ldg(sa_row + kc) : 0.0f;
-                const float f0 = sav * __ldg(sb0 + kc);
-                const float f1 = (EPI == MOE_EPI_SWIGLU_FP8) ? sav * __ldg(sb1 + kc) : f0;
+                cp_async_wait<2>();
+                __syncwarp();
+                const int slot = kc & 3;
+                const float sav = s.ring_sa[slot][et];
+                const float f0 = sav * s.ring_sb[slot][ew][0];
+                const float f1 = sav * s.ring_sb[slot][ew][1];
+                prefetch(kc + 3);
                 if (!mbar_wait(&s.tfull[b], bph, abort, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN + half * 128;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    uint32_t v[32];
-                    tmem_ld32(taddr + r * 32, v);
+                for (int r = 0; r < 2; ++r) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(taddr + r * 64, v0);
+                    tmem_ld32(taddr + r * 64 + 32, v1);
                     tmem_ld_wait();
-                    tmem_reg_fence(v);
-                    const float f = (r < 2) ? f0 : f1;
+                    tmem_reg_fence(v0);
+                    tmem_reg_fence(v1);
+                    const float f = (r == 0) ? f0 : f1;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[r * 32 + i] = fmaf(f, __uint_as_float(v[i]), acc[r * 32 + i]);
+                    for (int i = 0; i < 16; ++i) {
+                        ffma2(acc[r * 64 + 2 * i], acc[r * 64 + 2 * i + 1], v0[2 * i], v0[2 * i + 1], f);
+                        ffma2(acc[r * 64 + 32 + 2 * i], acc[r * 64 + 32 + 2 * i + 1], v1[2 * i], v1[2 * i + 1], f);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.tempty[b]);
             }
+            cp_async_wait<0>();
             if (!ok) break;
-            if (EPI == MOE_EPI_BF16) {
+            if (EPI == MOE_EPI_F32) {
+                if (valid) {
+                    float* dst = static_cast<float*>(p.out) + row * p.N + nt * BN + half * 128;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        st_v8_b32(dst + 8 * i, __float_as_uint(acc[8 * i]), __float_as_uint(acc[8 * i + 1]),
+                                  __float_as_uint(acc[8 * i + 2]), __float_as_uint(acc[8 * i + 3]),
+                                  __float_as_uint(acc[8 * i + 4]), __float_as_uint(acc[8 * i + 5]),
+                                  __float_as_uint(acc[8 * i + 6]), __float_as_uint(acc[8 * i + 7]));
+                }
+            } else if (EPI == MOE_EPI_BF16) {
                 if (valid) {
                     uint16_t* dst = static_cast<uint16_t*>(p.out) + row * p.N + nt * BN + half * 128;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        uint4 w;
-                        w.x = pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]);
-                        w.y = pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]);
-                        w.z = pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]);
-                        w.w = pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]);
-                        reinterpret_cast<uint4*>(dst)[i] = w;
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        st_v8_b32(dst + 16 * i, pack_bf16x2(acc[16 * i + 0], acc[16 * i + 1]),
+                                  pack_bf16x2(acc[16 * i + 2], acc[16 * i + 3]),
+                                  pack_bf16x2(acc[16 * i + 4], acc[16 * i + 5]),
+                                  pack_bf16x2(acc[16 * i + 6], acc[16 * i + 7]),
+                                  pack_bf16x2(acc[16 * i + 8], acc[16 * i + 9]),
+                                  pack_bf16x2(acc[16 * i + 10], acc[16 * i + 11]),
+                                  pack_bf16x2(acc[16 * i + 12], acc[16 * i + 13]),
+                                  pack_bf16x2(acc[16 * i + 14], acc[16 * i + 15]));
                 }
             } else {
                 // h = SiLU(gate) * up for this thread's 64 columns; gate in acc[0,64), up in acc[64,128)
@@ -272,7 +311,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float gte = acc[c];
-                    const float h = __fdiv_rn(gte, 1.0f + expf(-gte)) * acc[64 + c];
+                    const float h = gte * __frcp_rn(1.0f + __expf(-gte)) * acc[64 + c];
                     acc[c] = h;
                     amax = fmaxf(amax, fabsf(h));
                 }

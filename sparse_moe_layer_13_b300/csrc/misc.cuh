@@ -7,8 +7,8 @@ namespace moe {
 
 // y[t] = shared[t] + sum_k gate[t][k] * routed[row_of[t][k]] (+ residual[t]),
 // FP32 accumulation in that order, bf16 result (《DeepSeek-V3 Technical
-// Report》深度解读报告 §2.2). One CTA per token, 8 bf16 (16 bytes) per step.
-__global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict__ routed, const uint16_t* __restrict__ shared,
+// Report》深度解读报告 §2.2). One CTA per token, 4 FP32 (16 bytes) per step.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ routed, const float* __restrict__ shared,
                                                       const int32_t* __restrict__ row_of, const float* __restrict__ gate,
                                                       const uint16_t* __restrict__ residual, int T, int K, int d,
                                                       uint16_t* __restrict__ y) {
@@ -24,29 +24,23 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t* __restrict
         gates[threadIdx.x] = g;
     }
     __syncthreads();
-    const int nv = d / 8;
+    const int nv = d / 4;
     for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-        float acc[8];
-        const uint4 sh = __ldg(reinterpret_cast<const uint4*>(shared + static_cast<int64_t>(t) * d) + v);
-        acc[0] = bf16_lo(sh.x); acc[1] = bf16_hi(sh.x); acc[2] = bf16_lo(sh.y); acc[3] = bf16_hi(sh.y);
-        acc[4] = bf16_lo(sh.z); acc[5] = bf16_hi(sh.z); acc[6] = bf16_lo(sh.w); acc[7] = bf16_hi(sh.w);
+        float4 acc = __ldg(reinterpret_cast<const float4*>(shared + static_cast<int64_t>(t) * d) + v);
         for (int k = 0; k < K; ++k) {
             const float g = gates[k];
-            const uint4 u = __ldg(reinterpret_cast<const uint4*>(routed + static_cast<int64_t>(rows[k]) * d) + v);
-            acc[0] = fmaf(g, bf16_lo(u.x), acc[0]); acc[1] = fmaf(g, bf16_hi(u.x), acc[1]);
-            acc[2] = fmaf(g, bf16_lo(u.y), acc[2]); acc[3] = fmaf(g, bf16_hi(u.y), acc[3]);
-            acc[4] = fmaf(g, bf16_lo(u.z), acc[4]); acc[5] = fmaf(g, bf16_hi(u.z), acc[5]);
-            acc[6] = fmaf(g, bf16_lo(u.w), acc[6]); acc[7] = fmaf(g, bf16_hi(u.w), acc[7]);
+            const float4 u = __ldg(reinterpret_cast<const float4*>(routed + static_cast<int64_t>(rows[k]) * d) + v);
+            acc.x = fmaf(g, u.x, acc.x); acc.y = fmaf(g, u.y, acc.y);
+            acc.z = fmaf(g, u.z, acc.z); acc.w = fmaf(g, u.w, acc.w);
         }
         if (residual != nullptr) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4*>(residual + static_cast<int64_t>(t) * d) + v);
-            acc[0] += bf16_lo(u.x); acc[1] += bf16_hi(u.x); acc[2] += bf16_lo(u.y); acc[3] += bf16_hi(u.y);
-            acc[4] += bf16_lo(u.z); acc[5] += bf16_hi(u.z); acc[6] += bf16_lo(u.w); acc[7] += bf16_hi(u.w);
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(residual + static_cast<int64_t>(t) * d) + v);
+            acc.x += bf16_lo(u.x); acc.y += bf16_hi(u.x); acc.z += bf16_lo(u.y); acc.w += bf16_hi(u.y);
         }
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]); o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]); o.w = pack_bf16x2(acc[6], acc[7]);
-        reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * d)[v] = o;
+        uint2 o;
+        o.x = pack_bf16x2(acc.x, acc.y);
+        o.y = pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2*>(y + static_cast<int64_t>(t) * d)[v] = o;
     }
 }
 

@@ -11,6 +11,7 @@
 #include "permute.cuh"
 #include "quant.cuh"
 #include "route.cuh"
+#include "route_tc.cuh"
 
 namespace {
 
@@ -49,17 +50,35 @@ int num_sms() {
     return sms;
 }
 
-// Workspace layout: [route logits f32 T*E][per-block counts i32 nblk*E]
-// [per-block bases i32 nblk*E][offsets scratch i32 E+2]
+// K split of the router logits GEMM. Each split accumulates at most
+// rtc::kMaxChunksPerSplit chunks in TMEM (the tensor-core accumulation of a
+// long contraction drifts further from a correctly rounded FP32 sum than a
+// short one; the splits are added in FP32 by the selection kernel), and
+// small batches split further so the CTAs cover the SMs. Every split gets
+// at least one chunk.
+int route_ksplit(const moe_config* c) {
+    const int64_t ctas = ceil_div(c->T, rtc::BM) * ceil_div(c->E, rtc::BN_MAX);
+    const int nchunks = 3 * (c->d / rtc::BK);
+    const int ks_acc = (nchunks + rtc::kMaxChunksPerSplit - 1) / rtc::kMaxChunksPerSplit;
+    const int ks_fill = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(16, num_sms() / std::max<int64_t>(ctas, 1))));
+    int ks = std::min(std::max(ks_acc, ks_fill), nchunks);
+    const int per = (nchunks + ks - 1) / ks;
+    return (nchunks + per - 1) / per;
+}
+
+// Workspace layout: [router logit partials f32 ksplit*T*E][router weight
+// planes bf16 3*E*d][per-block counts i32 nblk*E][per-block bases i32
+// nblk*E][offsets scratch i32 E+2]
 struct WsLayout {
-    size_t logits, blk_counts, blk_base, offsets, total;
+    size_t logits, planes, blk_counts, blk_base, offsets, total;
 };
 
 WsLayout ws_layout(const moe_config* c) {
     WsLayout w{};
     const int64_t nblk = ceil_div(c->T, perm::kTokPerBlk);
     w.logits = 0;
-    w.blk_counts = align_up(static_cast<size_t>(c->T) * c->E * sizeof(float), 256);
+    w.planes = align_up(static_cast<size_t>(route_ksplit(c)) * c->T * c->E * sizeof(float), 256);
+    w.blk_counts = w.planes + align_up(static_cast<size_t>(3) * c->E * c->d * sizeof(uint16_t), 256);
     w.blk_base = w.blk_counts + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
     w.offsets = w.blk_base + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
     w.total = w.offsets + align_up(static_cast<size_t>(c->E + 2) * sizeof(int32_t), 256);
@@ -95,6 +114,45 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D K-major bf16 matrix [outer][inner], box [box_outer][64 elements], 128-byte swizzle.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPL, int MAXGK>
+void launch_select_t(const moe_config* c, const float* z, int ks, const float* off, const float* bias, int32_t* idx,
+                     float* gate, int grid, size_t smem, cudaStream_t st) {
+    route::select_kernel<EPL, MAXGK><<<grid, route::kSelWarps * 32, smem, st>>>(z, ks, c->T, c->E, c->G, c->M, c->K,
+                                                                               c->gk, off, bias, idx, gate);
+}
+
+template <int EPL>
+void launch_select_e(const moe_config* c, const float* z, int ks, const float* off, const float* bias, int32_t* idx,
+                     float* gate, int grid, size_t smem, cudaStream_t st) {
+    if (c->gk <= 2) launch_select_t<EPL, 2>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+    else if (c->gk <= 4) launch_select_t<EPL, 4>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+    else launch_select_t<EPL, route::kMaxGK>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+}
+
+void launch_select(const moe_config* c, const float* z, int ks, const float* off, const float* bias, int32_t* idx,
+                   float* gate, int grid, size_t smem, cudaStream_t st) {
+    const int epl = (c->E + 31) / 32;
+    if (epl <= 1) launch_select_e<1>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+    else if (epl <= 2) launch_select_e<2>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+    else if (epl <= 4) launch_select_e<4>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+    else if (epl <= 8) launch_select_e<8>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+    else if (epl <= 16) launch_select_e<16>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+    else launch_select_e<32>(c, z, ks, off, bias, idx, gate, grid, smem, st);
 }
 
 template <int EPI>
@@ -161,13 +219,32 @@ moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr, 
     cudaStream_t st = as_stream(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float* z = reinterpret_cast<float*>(ws + wl.logits);
-    dim3 lg(static_cast<unsigned>(ceil_div(cfg->T, 64)), static_cast<unsigned>(ceil_div(cfg->E, 64)));
-    route::logits_simt_kernel<<<lg, 256, 0, st>>>(x, Wr, cfg->T, cfg->d, cfg->E, z);
+    uint16_t* planes = reinterpret_cast<uint16_t*>(ws + wl.planes);
+    const int64_t nw = static_cast<int64_t>(cfg->E) * cfg->d;
+    rtc::split_kernel<<<static_cast<unsigned>(ceil_div(nw, 256)), 256, 0, st>>>(Wr, nw, planes);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    const int ks = route_ksplit(cfg);
+    const int bn = std::min(cfg->E, rtc::BN_MAX);
+    CUtensorMap tx, tw;
+    if (!make_map_bf16(&tx, x, static_cast<uint64_t>(cfg->d), static_cast<uint64_t>(cfg->T), rtc::BM)) return MOE_ERR_CUDA;
+    if (!make_map_bf16(&tw, planes, static_cast<uint64_t>(cfg->d), static_cast<uint64_t>(3) * cfg->E,
+                       static_cast<uint32_t>(bn)))
+        return MOE_ERR_CUDA;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(rtc::logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(rtc::SMEM_BYTES)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set = true;
+    }
+    const dim3 lg(static_cast<unsigned>(ceil_div(cfg->T, rtc::BM)), static_cast<unsigned>(ceil_div(cfg->E, rtc::BN_MAX)),
+                  static_cast<unsigned>(ks));
+    rtc::Params rp{cfg->T, cfg->d, cfg->E, bn, ks, z};
+    rtc::logits_kernel<<<lg, rtc::NUM_THREADS, rtc::SMEM_BYTES, st>>>(tx, tw, rp);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     const size_t sel_smem = static_cast<size_t>(route::kSelWarps) * 2 * cfg->E * sizeof(float);
     const int sel_grid = static_cast<int>(std::min<int64_t>(ceil_div(cfg->T, route::kSelWarps), 65535));
-    route::select_kernel<<<sel_grid, route::kSelWarps * 32, sel_smem, st>>>(
-        z, cfg->T, cfg->E, cfg->G, cfg->M, cfg->K, cfg->gk, logit_offset, bias, topk_idx, topk_gate);
+    launch_select(cfg, z, ks, logit_offset, bias, topk_idx, topk_gate, sel_grid, sel_smem, st);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     if (counts != nullptr) {
         const int nblk = static_cast<int>(ceil_div(cfg->T, perm::kTokPerBlk));
@@ -189,9 +266,11 @@ moe_status moe_quant_fp8_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
     if (!x || !q || !scale || rows < 0 || cols < 0 || ld < cols) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || ld % 8) return MOE_ERR_INVALID_ARG;
     if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0 || cols == 0) return MOE_OK;
     const int64_t tiles = rows * (cols / 128);
-    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 8), static_cast<int64_t>(num_sms()) * 16));
+    // 8 warps per CTA, two tiles per warp step, two steps in flight per thread
+    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 32), static_cast<int64_t>(num_sms()) * 16));
     quant_1x128_kernel<<<grid, 256, 0, as_stream(stream)>>>(x, rows, cols, ld, q, scale);
     return launch_status();
 }
@@ -258,7 +337,7 @@ moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t 
                                 void* out, float* out_scale, void* stream) {
     if (!offsets || !A || !sa || !B || !sb || !out || rows < 0 || groups < 1 || N < 0 || Kdim < 0)
         return MOE_ERR_INVALID_ARG;
-    if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8) return MOE_ERR_INVALID_ARG;
+    if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8 && epilogue != MOE_EPI_F32) return MOE_ERR_INVALID_ARG;
     if (epilogue == MOE_EPI_SWIGLU_FP8 && !out_scale) return MOE_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
     if (groups > gemm::MAX_GROUPS || N % gemm::BN || N == 0 || Kdim % gemm::BK || Kdim == 0 || rows >= INT32_MAX)
@@ -273,10 +352,11 @@ moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t 
     const int64_t tiles_max = (ceil_div(rows, gemm::BM) + groups) * (N / gemm::BN);
     cudaStream_t st = as_stream(stream);
     if (epilogue == MOE_EPI_BF16) return launch_gemm<MOE_EPI_BF16>(ta, tb, p, tiles_max, st);
+    if (epilogue == MOE_EPI_F32) return launch_gemm<MOE_EPI_F32>(ta, tb, p, tiles_max, st);
     return launch_gemm<MOE_EPI_SWIGLU_FP8>(ta, tb, p, tiles_max, st);
 }
 
-moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const uint16_t* shared_out,
+moe_status moe_combine(const moe_config* cfg, const float* routed_out, const float* shared_out,
                        const int32_t* row_of, const float* topk_gate, const uint16_t* residual, uint16_t* y,
                        void* stream) {
     const moe_status cs = check_config(cfg);
@@ -284,7 +364,7 @@ moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const 
     if (!routed_out || !shared_out || !row_of || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
     if (!aligned16(routed_out) || !aligned16(shared_out) || !aligned16(y) || (residual && !aligned16(residual)))
         return MOE_ERR_INVALID_ARG;
-    combine_kernel<<<cfg->T, 128, 0, as_stream(stream)>>>(routed_out, shared_out, row_of, topk_gate, residual, cfg->T,
+    combine_kernel<<<cfg->T, 256, 0, as_stream(stream)>>>(routed_out, shared_out, row_of, topk_gate, residual, cfg->T,
                                                           cfg->K, cfg->d, y);
     return launch_status();
 }

@@ -8,29 +8,51 @@
 
 namespace moe {
 
-// One warp per 1x128 tile: 4 bf16 values per lane (8-byte loads), amax by
-// warp shuffle, 4 E4M3 codes per lane (4-byte stores). Grid-stride over
-// tiles, so any grid size is valid.
+// Half a warp per 1x128 tile: 8 bf16 values per lane (16-byte loads), amax
+// by shuffles inside the half warp, 8 E4M3 codes per lane (8-byte stores);
+// each warp step covers two tiles and a thread keeps two steps in flight.
+// Grid-stride over tile pairs, so any grid size is valid.
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                           int64_t cols, int64_t ld, uint8_t* __restrict__ q,
                                                           float* __restrict__ scale) {
     const int64_t tiles_per_row = cols / 128;
     const int64_t ntiles = rows * tiles_per_row;
+    const int64_t npairs = (ntiles + 1) / 2;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const uint32_t lane = lane_id();
-    for (int64_t t = warp; t < ntiles; t += nwarps) {
-        const int64_t r = t / tiles_per_row;
-        const int64_t c = t - r * tiles_per_row;
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(x + r * ld + c * 128) + lane);
-        const float v0 = bf16_lo(w.x), v1 = bf16_hi(w.x), v2 = bf16_lo(w.y), v3 = bf16_hi(w.y);
-        float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+    const uint32_t sub = lane & 15;
+    for (int64_t p0 = warp; p0 < npairs; p0 += 2 * nwarps) {
+        uint4 w[2];
+        int64_t tile[2];
+        bool live[2];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float s = __fdiv_rn(amax, kE4M3Max);
-        const uint32_t codes = e4m3x4(quant_ratio(v0, s), quant_ratio(v1, s), quant_ratio(v2, s), quant_ratio(v3, s));
-        reinterpret_cast<uint32_t*>(q + r * cols + c * 128)[lane] = codes;
-        if (lane == 0) scale[r * tiles_per_row + c] = s;
+        for (int u = 0; u < 2; ++u) {
+            tile[u] = 2 * (p0 + u * nwarps) + (lane >> 4);
+            live[u] = (p0 + u * nwarps) < npairs && tile[u] < ntiles;
+            w[u] = make_uint4(0, 0, 0, 0);
+            if (live[u]) {
+                const int64_t r = tile[u] / tiles_per_row, c = tile[u] - r * tiles_per_row;
+                w[u] = __ldg(reinterpret_cast<const uint4*>(x + r * ld + c * 128) + sub);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float v0 = bf16_lo(w[u].x), v1 = bf16_hi(w[u].x), v2 = bf16_lo(w[u].y), v3 = bf16_hi(w[u].y);
+            const float v4 = bf16_lo(w[u].z), v5 = bf16_hi(w[u].z), v6 = bf16_lo(w[u].w), v7 = bf16_hi(w[u].w);
+            float amax = fmaxf(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))),
+                               fmaxf(fmaxf(fabsf(v4), fabsf(v5)), fmaxf(fabsf(v6), fabsf(v7))));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (!live[u]) continue;
+            const float s = __fdiv_rn(amax, kE4M3Max);
+            const int64_t r = tile[u] / tiles_per_row, c = tile[u] - r * tiles_per_row;
+            uint2 codes;
+            codes.x = e4m3x4(quant_ratio(v0, s), quant_ratio(v1, s), quant_ratio(v2, s), quant_ratio(v3, s));
+            codes.y = e4m3x4(quant_ratio(v4, s), quant_ratio(v5, s), quant_ratio(v6, s), quant_ratio(v7, s));
+            reinterpret_cast<uint2*>(q + r * cols + c * 128)[sub] = codes;
+            if (sub == 0) scale[r * tiles_per_row + c] = s;
+        }
     }
 }
 

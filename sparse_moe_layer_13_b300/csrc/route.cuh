@@ -1,6 +1,7 @@
 // Router kernels (《DeepSeek-V3 Technical Report》深度解读报告 §2.2-§2.4).
 //
-//  * route_select_kernel: one warp per token. Lane l holds experts l, l+32,
+//  * select_kernel: one warp per token; the logits arrive as K-split FP32
+//    partials z[s][t][e], summed in split order. Lane l holds experts l, l+32,
 //    ... (coalesced logit loads). s = sigmoid(z + o), s' = s + b. Lane g < G
 //    scans group g's biased affinities and sums its gk largest; groups are
 //    ranked by shuffles (equal scores: lower index first) and the top M kept;
@@ -18,8 +19,12 @@ constexpr int kMaxEPL = 32;      // experts per lane: E <= 1024
 constexpr int kMaxGK = 16;
 constexpr int kSelWarps = 4;     // tokens per CTA of the select kernel
 
+// EPL: experts per lane (>= ceil(E/32)); MAXGK: >= gk (length of the
+// per-group insertion list). Both compile-time so the per-lane arrays stay
+// in registers.
+template <int EPL, int MAXGK>
 __global__ void __launch_bounds__(kSelWarps * 32)
-select_kernel(const float* __restrict__ z, int T, int E, int G, int M, int K, int gk,
+select_kernel(const float* __restrict__ z, int ksplit, int T, int E, int G, int M, int K, int gk,
               const float* __restrict__ offset, const float* __restrict__ bias,
               int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate) {
     extern __shared__ float sel_smem[];          // [kSelWarps][2][E]: biased, raw
@@ -28,16 +33,18 @@ select_kernel(const float* __restrict__ z, int T, int E, int G, int M, int K, in
     float* sp = sel_smem + static_cast<size_t>(w) * 2 * E;
     float* sr = sp + E;
     const int n = E / G;
-    const int epl = (E + 31) / 32;
+    const int64_t TE = static_cast<int64_t>(T) * E;
     for (int t = blockIdx.x * kSelWarps + w; t < T; t += gridDim.x * kSelWarps) {
         const float* zt = z + static_cast<int64_t>(t) * E;
-        float sb[kMaxEPL];
+        float sb[EPL];
 #pragma unroll
-        for (int i = 0; i < kMaxEPL; ++i) {
+        for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
             sb[i] = -INFINITY;
-            if (i < epl && e < E) {
+            if (e < E) {
                 float zz = __ldg(zt + e);
+                for (int sp_i = 1; sp_i < ksplit; ++sp_i)       // K-split partials, fixed order
+                    zz += __ldg(zt + sp_i * TE + e);
                 if (offset != nullptr) zz += __ldg(offset + e);
                 const float s = __fdiv_rn(1.0f, 1.0f + expf(-zz));
                 sb[i] = s + __ldg(bias + e);
@@ -49,19 +56,19 @@ select_kernel(const float* __restrict__ z, int T, int E, int G, int M, int K, in
         // group scores: sum of the gk largest biased affinities of each group
         float score = -INFINITY;
         if (lane < G) {
-            float top[kMaxGK];
+            float top[MAXGK];
 #pragma unroll
-            for (int j = 0; j < kMaxGK; ++j) top[j] = -INFINITY;
+            for (int j = 0; j < MAXGK; ++j) top[j] = -INFINITY;
             for (int e = lane * n; e < (lane + 1) * n; ++e) {
                 float v = sp[e];
 #pragma unroll
-                for (int j = 0; j < kMaxGK; ++j) {      // insertion into a descending list
+                for (int j = 0; j < MAXGK; ++j) {      // insertion into a descending list
                     if (j < gk && v > top[j]) { const float tmp = top[j]; top[j] = v; v = tmp; }
                 }
             }
             score = 0.0f;
 #pragma unroll
-            for (int j = 0; j < kMaxGK; ++j) if (j < gk) score += top[j];
+            for (int j = 0; j < MAXGK; ++j) if (j < gk) score += top[j];
         }
         int rank = 0;
         for (int g2 = 0; g2 < G; ++g2) {
@@ -71,9 +78,9 @@ select_kernel(const float* __restrict__ z, int T, int E, int G, int M, int K, in
         const uint32_t keep = __ballot_sync(0xffffffffu, lane < G && rank < M);
         // drop experts of groups that were not kept
 #pragma unroll
-        for (int i = 0; i < kMaxEPL; ++i) {
+        for (int i = 0; i < EPL; ++i) {
             const int e = lane + 32 * i;
-            if (i < epl && e < E && !((keep >> (e / n)) & 1u)) sb[i] = -INFINITY;
+            if (e < E && !((keep >> (e / n)) & 1u)) sb[i] = -INFINITY;
         }
         int my_e = 0;
         float my_s = 0.0f;
@@ -81,8 +88,8 @@ select_kernel(const float* __restrict__ z, int T, int E, int G, int M, int K, in
             float bv = -INFINITY;
             int be = 0x7fffffff, bi = -1;
 #pragma unroll
-            for (int i = 0; i < kMaxEPL; ++i) {
-                if (i < epl && sb[i] > bv) { bv = sb[i]; be = lane + 32 * i; bi = i; }
+            for (int i = 0; i < EPL; ++i) {
+                if (sb[i] > bv) { bv = sb[i]; be = lane + 32 * i; bi = i; }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -90,9 +97,9 @@ select_kernel(const float* __restrict__ z, int T, int E, int G, int M, int K, in
                 const int oe = __shfl_xor_sync(0xffffffffu, be, o);
                 if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
             }
-            if ((be & 31) == lane && bi >= 0 && lane + 32 * bi == be) {
+            if (bi >= 0 && lane + 32 * bi == be) {
 #pragma unroll
-                for (int i = 0; i < kMaxEPL; ++i) if (i == bi) sb[i] = -INFINITY;
+                for (int i = 0; i < EPL; ++i) if (i == bi) sb[i] = -INFINITY;
             }
             if (lane == k) { my_e = be; my_s = sr[be]; }
         }
@@ -104,44 +111,6 @@ select_kernel(const float* __restrict__ z, int T, int E, int G, int M, int K, in
         }
         __syncwarp();
     }
-}
-
-// Router logits on the CUDA cores in FP32: z[t][e] = sum_j x[t][j] * Wr[e][j].
-// 64x64 output tile per CTA, K step 32, 4x4 outputs per thread.
-__global__ void __launch_bounds__(256) logits_simt_kernel(const uint16_t* __restrict__ x, const float* __restrict__ Wr,
-                                                          int T, int d, int E, float* __restrict__ z) {
-    __shared__ float xs[32][64 + 4];
-    __shared__ float ws[32][64 + 4];
-    const int t0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < d; k0 += 32) {
-        for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-            const int r = i >> 5, c = i & 31;
-            const int t = t0 + r, e = e0 + r;
-            xs[c][r] = (t < T) ? __uint_as_float(static_cast<uint32_t>(x[static_cast<int64_t>(t) * d + k0 + c]) << 16) : 0.0f;
-            ws[c][r] = (e < E) ? Wr[static_cast<int64_t>(e) * d + k0 + c] : 0.0f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int c = 0; c < 32; ++c) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) { a[i] = xs[c][ty * 4 + i]; b[i] = ws[c][tx * 4 + i]; }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int t = t0 + ty * 4 + i, e = e0 + tx * 4 + j;
-            if (t < T && e < E) z[static_cast<int64_t>(t) * E + e] = acc[i][j];
-        }
 }
 
 }  // namespace route

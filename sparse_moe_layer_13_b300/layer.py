@@ -70,7 +70,7 @@ class MoELayer:
         }
         self.hq = z(R, I, dt=torch.uint8)
         self.hs = z(R, I // 128, dt=torch.float32)
-        self.out = z(R, d, dt=torch.bfloat16)
+        self.out = z(R, d, dt=torch.float32)
         self.y = z(T, d, dt=torch.bfloat16)
 
     def forward(self, x: torch.Tensor, residual: bool = False, update_bias: bool = True,
@@ -95,7 +95,7 @@ class MoELayer:
             ev["gemm1"][1].record()
         if "gemm2" in ev:
             ev["gemm2"][0].record()
-        B.grouped_gemm_fp8(self.perm["offsets"], self.hq, self.hs, self.w.q2, self.w.s2, B.MOE_EPI_BF16, self.out)
+        B.grouped_gemm_fp8(self.perm["offsets"], self.hq, self.hs, self.w.q2, self.w.s2, B.MOE_EPI_F32, self.out)
         if "gemm2" in ev:
             ev["gemm2"][1].record()
         TK = c.T * c.K
@@ -106,5 +106,6 @@ class MoELayer:
             B.bias_update(c.E, c.T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
         return self.y
 
-    # launches per forward: route 2 (+2 with counts), quant 1, permute 4, GEMMs 2, combine 1, bias 1
-    LAUNCHES_PER_FORWARD = 13
+    # library kernel launches per forward: route 5 (weight split, logits, selection, histogram,
+    # scan), quantise 1, permute 4, grouped GEMMs 2, combine 1, bias update 1
+    LAUNCHES_PER_FORWARD = 14

@@ -43,6 +43,7 @@ def y_metrics(got: np.ndarray, want: np.ndarray):
 
 def assert_y_close(got, want):
     rel, mx = y_metrics(got, want)
+    print(f"[parity] rel-L2 {rel:.3e}  max-abs/RMS {mx:.3e}  over {got.shape[0]} tokens")
     assert rel <= Y_REL_L2, f"rel-L2 {rel:.3e}"
     assert mx <= Y_MAX_RMS, f"max-abs/RMS {mx:.3e}"
     return rel, mx

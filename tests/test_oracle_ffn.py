@@ -91,4 +91,4 @@ def test_expert_matches_scalar_brute_force():
         H = dequant_1x128(hq, hs)[0]
         for n in range(0, d, 17):
             o = math.fsum(H[j] * W2[n, j] for j in range(I))
-            assert abs(out[m, n] - float(round_bf16(o))) <= 2.0 ** -7 * abs(o) + 1e-30
+            assert abs(out[m, n] - o) <= 1e-12 * abs(o) + 1e-15

@@ -6,7 +6,6 @@ import math
 import numpy as np
 import pytest
 
-from oracle.ffn import round_bf16
 from oracle.layer import Layer
 from oracle.quant import dequant_128x128, dequant_1x128, quant_1x128
 from sparse_moe_layer_13_b300.configs import MoEConfig
@@ -42,12 +41,12 @@ def _brute_token(cfg, x, Wr, b, layer, t):
             math.fsum(X * W1[j]), math.fsum(X * W3[j]))) for j in range(cfg.I)], np.float32)
         hq, hs = quant_1x128(h[None, :])
         H = dequant_1x128(hq, hs)[0]
-        return np.array([float(round_bf16(math.fsum(H * W2[i]))) for i in range(cfg.d)])
+        return np.array([math.fsum(H * W2[i]) for i in range(cfg.d)])
 
     y = ffn(cfg.E)
     for e in chosen:
         y = y + (s[e] / tot) * ffn(e)
-    return set(chosen), round_bf16(y)
+    return set(chosen), y
 
 
 def test_layer_matches_scalar_brute_force():
@@ -57,7 +56,8 @@ def test_layer_matches_scalar_brute_force():
     for t in range(CFG.T):
         chosen, y = _brute_token(CFG, x, Wr, b, layer, t)
         assert set(res["idx"][t]) == chosen
-        assert np.max(np.abs(res["y"][t] - y)) <= 2.0 ** -7 * np.max(np.abs(y))
+        # the two sums of h may round to float32 differently in the last place
+        assert np.max(np.abs(res["y"][t] - y)) <= 1e-6 * np.max(np.abs(y))
 
 
 def test_all_experts_special_case():
@@ -72,7 +72,7 @@ def test_all_experts_special_case():
     y = expert_forward(xq, xs, layer.expert(4))
     for e in range(4):
         y = y + g[:, e:e + 1] * expert_forward(xq, xs, layer.expert(e))
-    np.testing.assert_allclose(res["y"], round_bf16(y), rtol=2.0 ** -7, atol=1e-6)
+    np.testing.assert_allclose(res["y"], y, rtol=1e-12, atol=1e-12)
 
 
 def test_tokens_are_independent_and_subset_matches():
@@ -91,4 +91,4 @@ def test_residual_adds_input():
     layer = Layer(CFG, Wr, b, lambda e: wts[e])
     y0 = layer.forward(x)["y"]
     y1 = layer.forward(x, residual=True)["y"]
-    np.testing.assert_allclose(y1, y0 + x, rtol=2.0 ** -7, atol=2.0 ** -7 * np.abs(x).max())
+    np.testing.assert_allclose(y1, y0 + x, rtol=1e-12, atol=1e-12)
