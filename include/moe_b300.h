@@ -165,6 +165,30 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx,
                        uint8_t* xq_perm, float* xs_perm,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* moe_permute without a workspace, for callers that cannot allocate device
+ * memory: for example a host framework that owns every allocation and hands
+ * this library only the input and output buffers of a call, or a serving
+ * loop that forbids allocation after start-up. The pages have no
+ * counterpart; this is a packaging variant of moe_permute with the same
+ * arguments (minus the workspace) and bit-identical results.
+ * Scratch: a file-scope device array of 1 MiB (262144 int32) inside the
+ * library, held by every device that loads the library until the process
+ * exits. It bounds the shape: 2 * ceil(T / 256) * E must not exceed 262144
+ * (e.g. T <= 131072 tokens for E = 256), otherwise MOE_ERR_UNSUPPORTED_SHAPE
+ * and nothing is launched. Allocates nothing and calls no allocating
+ * routine.
+ * The first call on each device looks up the array's device address with
+ * cudaGetSymbolAddress (that device must be current) and caches it; make that
+ * first call before any stream capture.
+ * All calls share the one array: two calls that overlap on the GPU (e.g. on
+ * different streams without ordering between them) race and give wrong
+ * results. Each call writes every scratch entry it reads, so what an
+ * earlier call left behind never matters. */
+moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx,
+                               const uint8_t* xq, const float* xs,
+                               int32_t* offsets, int32_t* counts, int32_t* sorted_token, int32_t* row_of,
+                               uint8_t* xq_perm, float* xs_perm, void* stream);
+
 /* Grouped FP8 GEMM with per-chunk scale promotion
  * ("DeepSeek-V3的MoE架构设计革新" §2 items 1-2): for each group g and row r in
  * [offsets[g], offsets[g+1]),

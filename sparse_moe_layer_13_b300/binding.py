@@ -40,6 +40,7 @@ _SIG = {
     "moe_quant_fp8_128x128": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P]),
     "moe_pack_w13": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_permute_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_gemm_fp8": (ctypes.c_int, [_I32, _P, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_bias_update": (ctypes.c_int, [_I32, _I32, _I32, _P, ctypes.c_float, _P, _P]),
@@ -190,6 +191,33 @@ def permute(cfg, idx, xq, xs, workspace=None, out=None, want_counts=False):
     _call("moe_permute", ctypes.byref(c), _ptr(idx), _ptr(xq), _ptr(xs), _ptr(out["offsets"]), _ptr(out["counts"]),
           _ptr(out["sorted_token"]), _ptr(out["row_of"]), _ptr(out["xq_perm"]), _ptr(out["xs_perm"]),
           _ptr(workspace), workspace.numel(), _stream())
+    return out
+
+
+def permute_noalloc(cfg, idx, xq, xs, out=None, want_counts=False):
+    """moe_permute_noalloc: same results as permute(), scratch held inside the library.
+
+    Outputs are allocated here only when the caller passes none; the library
+    call itself allocates nothing.
+    """
+    dev = idx.device
+    _need(idx, torch.int32, "topk_idx", (cfg.T, cfg.K))
+    _need(xq, torch.uint8, "xq", (cfg.T, cfg.d))
+    _need(xs, torch.float32, "xs", (cfg.T, cfg.d // 128))
+    rows = cfg.rows
+    if out is None:
+        out = {
+            "offsets": torch.empty(cfg.E + 2, dtype=torch.int32, device=dev),
+            "counts": torch.empty(cfg.E, dtype=torch.int32, device=dev) if want_counts else None,
+            "sorted_token": torch.empty(cfg.T * cfg.K, dtype=torch.int32, device=dev),
+            "row_of": torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev),
+            "xq_perm": torch.empty(rows, cfg.d, dtype=torch.uint8, device=dev),
+            "xs_perm": torch.empty(rows, cfg.d // 128, dtype=torch.float32, device=dev),
+        }
+    c = config_c(cfg)
+    _call("moe_permute_noalloc", ctypes.byref(c), _ptr(idx), _ptr(xq), _ptr(xs), _ptr(out["offsets"]),
+          _ptr(out["counts"]), _ptr(out["sorted_token"]), _ptr(out["row_of"]), _ptr(out["xq_perm"]),
+          _ptr(out["xs_perm"]), _stream())
     return out
 
 

@@ -181,6 +181,35 @@ const char* kStatusNames[] = {
     "MOE_ERR_NO_DEVICE: no usable sm_103 device",
 };
 
+// ---------------------------------------------------------------------------
+// Static scratch of moe_permute_noalloc: the per-block expert counts and
+// per-block starting rows (2 * nblk * E int32) live in this file-scope device
+// array instead of a caller workspace. Every device that loads the library
+// holds it until the process exits.
+constexpr size_t kPermuteScratchInts = 256 * 1024;   // 1 MiB
+static __device__ __align__(256) int32_t g_permute_scratch[kPermuteScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+int32_t* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_permute_scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address is asked of the
+// runtime once per device (with that device current) and cached.
+moe_status permute_scratch(int32_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+        g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -325,6 +354,41 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, const uin
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     perm::scatter_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E, blk_base, row_of,
                                                                sorted_token);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    const int64_t rows = npairs + cfg->T;
+    perm::gather_kernel<<<static_cast<unsigned>(ceil_div(rows * 32, 256)), 256, 0, st>>>(
+        sorted_token, cfg->T, cfg->K, cfg->d, xq, xs, xq_perm, xs_perm);
+    return launch_status();
+}
+
+moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, const uint8_t* xq, const float* xs,
+                               int32_t* offsets, int32_t* counts, int32_t* sorted_token, int32_t* row_of,
+                               uint8_t* xq_perm, float* xs_perm, void* stream) {
+    const moe_status cs = check_config(cfg);
+    if (cs != MOE_OK) return cs;
+    const int64_t nblk = ceil_div(cfg->T, perm::kTokPerBlk);
+    if (2 * nblk * cfg->E > static_cast<int64_t>(kPermuteScratchInts)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!topk_idx || !xq || !xs || !offsets || !sorted_token || !row_of || !xq_perm || !xs_perm)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(xq_perm) || !aligned16(topk_idx)) return MOE_ERR_INVALID_ARG;
+    int32_t* scratch = nullptr;
+    const moe_status ss = permute_scratch(&scratch);
+    if (ss != MOE_OK) return ss;
+    // every scratch entry is written by the histogram and scan kernels before
+    // it is read, so nothing left by an earlier call needs clearing
+    int32_t* blk_counts = scratch;
+    int32_t* blk_base = scratch + nblk * cfg->E;
+    cudaStream_t st = as_stream(stream);
+    const int64_t npairs = static_cast<int64_t>(cfg->T) * cfg->K;
+    const size_t hsm = static_cast<size_t>(perm::kWarps) * cfg->E * sizeof(int);
+    perm::hist_kernel<<<static_cast<unsigned>(nblk), perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E,
+                                                                                   blk_counts);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    perm::scan_kernel<<<1, 1024, 0, st>>>(blk_counts, static_cast<int>(nblk), cfg->E, cfg->T, cfg->K, blk_base,
+                                          offsets, counts);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    perm::scatter_kernel<<<static_cast<unsigned>(nblk), perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E,
+                                                                                      blk_base, row_of, sorted_token);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     const int64_t rows = npairs + cfg->T;
     perm::gather_kernel<<<static_cast<unsigned>(ceil_div(rows * 32, 256)), 256, 0, st>>>(
