@@ -73,7 +73,11 @@ typedef enum moe_epilogue {
      * out_scale: f32 [rows][N/256]. */
     MOE_EPI_SWIGLU_FP8 = 1,
     /* out: f32 [rows][N]. */
-    MOE_EPI_F32 = 2
+    MOE_EPI_F32 = 2,
+    /* out: bf16 [rows][N] for every group but the last; out_aux: f32
+     * [offsets[groups] - offsets[groups-1]][N] for the last group (the
+     * shared expert, whose output enters the layer output with gate 1). */
+    MOE_EPI_BF16_F32_LAST = 3
 } moe_epilogue;
 
 /* Human-readable name of a status. Never NULL. */
@@ -200,7 +204,13 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx,
  *   rows      rows of A and of the output
  *   A, sa     device u8 [rows][Kdim], f32 [rows][Kdim/128]
  *   B, sb     device u8 [groups][N][Kdim], f32 [groups][N/128][Kdim/128]
- *   epilogue  moe_epilogue; out / out_scale as described there
+ *   epilogue  moe_epilogue; out / out_aux as described there
+ * The SwiGLU epilogue computes h = SiLU(gate) * up in FP32 with the fast
+ * exponential and division and quantises it per 1x128 tile with the scale
+ * rule above, multiplying by the correctly rounded reciprocal of the scale;
+ * h therefore matches an exact evaluation to a few FP32 ulps, not bit for
+ * bit, and its E4M3 codes match except where that difference crosses a
+ * rounding boundary.
  * N % 256 == 0, Kdim % 128 == 0. Rows outside every group are not written.
  * Runs on the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA
  * operand loads); no workspace. */
@@ -208,18 +218,18 @@ moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t 
                                 int32_t N, int32_t Kdim,
                                 const uint8_t* A, const float* sa,
                                 const uint8_t* B, const float* sb,
-                                int32_t epilogue, void* out, float* out_scale, void* stream);
+                                int32_t epilogue, void* out, float* out_aux, void* stream);
 
 /* Gate-weighted un-permute and combine (《DeepSeek-V3 Technical Report》深度解读报告
  * §2.2): y[t] = shared_out[t] + sum_k topk_gate[t][k] * routed_out[row_of[t][k]]
  * (+ residual[t] if residual != NULL), accumulated in FP32 in that order,
  * rounded to bf16.
- *   routed_out device f32 [T*K][d]; shared_out device f32 [T][d]
- *   (the expert outputs of moe_grouped_gemm_fp8 with MOE_EPI_F32)
+ *   routed_out device bf16 [T*K][d]; shared_out device f32 [T][d]
+ *   (the expert outputs of moe_grouped_gemm_fp8 with MOE_EPI_BF16_F32_LAST)
  *   row_of     device i32 [T][K] (values in [0, T*K), else MOE_ERR_DEVICE_CHECK)
  *   topk_gate  device f32 [T][K]; residual device bf16 [T][d] or NULL
  *   y          device bf16 [T][d] out */
-moe_status moe_combine(const moe_config* cfg, const float* routed_out, const float* shared_out,
+moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const float* shared_out,
                        const int32_t* row_of, const float* topk_gate, const uint16_t* residual,
                        uint16_t* y, void* stream);
 

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
 MOE_EPI_BF16 = 0
 MOE_EPI_SWIGLU_FP8 = 1
 MOE_EPI_F32 = 2
+MOE_EPI_BF16_F32_LAST = 3
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE",
@@ -221,8 +222,12 @@ def permute_noalloc(cfg, idx, xq, xs, out=None, want_counts=False):
     return out
 
 
-def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out_scale=None):
-    """offsets i32 [G+1]; A u8 [rows][K]; sa f32 [rows][K/128]; B u8 [G][N][K]; sb f32 [G][N/128][K/128]."""
+def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out_scale=None, last_rows=None):
+    """offsets i32 [G+1]; A u8 [rows][K]; sa f32 [rows][K/128]; B u8 [G][N][K]; sb f32 [G][N/128][K/128].
+
+    out_scale is the auxiliary output: h scales for the SwiGLU epilogue, or
+    the FP32 output of the last group (last_rows rows) for MOE_EPI_BF16_F32_LAST.
+    """
     groups = offsets.numel() - 1
     rows, Kdim = A.shape
     N = B.shape[1]
@@ -233,6 +238,10 @@ def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out
     _need(sb, torch.float32, "sb", (groups, N // 128, Kdim // 128))
     if epilogue == MOE_EPI_BF16:
         out = torch.empty(rows, N, dtype=torch.bfloat16, device=A.device) if out is None else out
+    elif epilogue == MOE_EPI_BF16_F32_LAST:
+        out = torch.empty(rows, N, dtype=torch.bfloat16, device=A.device) if out is None else out
+        if out_scale is None:
+            out_scale = torch.empty(last_rows, N, dtype=torch.float32, device=A.device)
     elif epilogue == MOE_EPI_F32:
         out = torch.empty(rows, N, dtype=torch.float32, device=A.device) if out is None else out
     else:
@@ -245,8 +254,8 @@ def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out
 
 
 def combine(cfg, routed_out, shared_out, row_of, gate, residual=None, y=None):
-    """routed_out f32 [T*K][d], shared_out f32 [T][d] -> y bf16 [T][d]."""
-    _need(routed_out, torch.float32, "routed_out", (cfg.T * cfg.K, cfg.d))
+    """routed_out bf16 [T*K][d], shared_out f32 [T][d] -> y bf16 [T][d]."""
+    _need(routed_out, torch.bfloat16, "routed_out", (cfg.T * cfg.K, cfg.d))
     _need(shared_out, torch.float32, "shared_out", (cfg.T, cfg.d))
     _need(row_of, torch.int32, "row_of", (cfg.T, cfg.K))
     _need(gate, torch.float32, "topk_gate", (cfg.T, cfg.K))

@@ -76,7 +76,7 @@ struct Params {
     const float* sa;
     const float* sb;
     void* out;
-    float* out_scale;
+    float* out_aux;      // SwiGLU: h scales; BF16_F32_LAST: FP32 output of the last group
 };
 
 // tile -> (group, row tile inside the group, column tile)
@@ -245,9 +245,9 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             prefetch(0);
             prefetch(1);
             prefetch(2);
-            float acc[128];
+            float2 acc2[64];             // FP32 tile accumulator, column pairs
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
             for (int kc = 0; kc < nkc; ++kc, ++it) {
                 const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
                 cp_async_wait<2>();
@@ -268,11 +268,13 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     tmem_ld_wait();
                     tmem_reg_fence(v0);
                     tmem_reg_fence(v1);
-                    const float f = (r == 0) ? f0 : f1;
+                    const float2 ff = make_float2((r == 0) ? f0 : f1, (r == 0) ? f0 : f1);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        ffma2(acc[r * 64 + 2 * i], acc[r * 64 + 2 * i + 1], v0[2 * i], v0[2 * i + 1], f);
-                        ffma2(acc[r * 64 + 32 + 2 * i], acc[r * 64 + 32 + 2 * i + 1], v1[2 * i], v1[2 * i + 1], f);
+                        acc2[r * 32 + i] = __ffma2_rn(make_float2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1])),
+                                                      ff, acc2[r * 32 + i]);
+                        acc2[r * 32 + 16 + i] = __ffma2_rn(make_float2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1])),
+                                                           ff, acc2[r * 32 + 16 + i]);
                     }
                 }
                 tc_fence_before();
@@ -280,10 +282,14 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 if (lane == 0) mbar_arrive(&s.tempty[b]);
             }
             cp_async_wait<0>();
+            float* acc = reinterpret_cast<float*>(acc2);
             if (!ok) break;
-            if (EPI == MOE_EPI_F32) {
+            const bool f32_out = (EPI == MOE_EPI_F32) || (EPI == MOE_EPI_BF16_F32_LAST && g == groups - 1);
+            if (f32_out) {
                 if (valid) {
-                    float* dst = static_cast<float*>(p.out) + row * p.N + nt * BN + half * 128;
+                    float* dst = (EPI == MOE_EPI_F32)
+                                     ? static_cast<float*>(p.out) + row * p.N + nt * BN + half * 128
+                                     : p.out_aux + (row - s.row_start[g]) * p.N + nt * BN + half * 128;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         st_v8_b32(dst + 8 * i, __float_as_uint(acc[8 * i]), __float_as_uint(acc[8 * i + 1]),
@@ -291,7 +297,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                                   __float_as_uint(acc[8 * i + 4]), __float_as_uint(acc[8 * i + 5]),
                                   __float_as_uint(acc[8 * i + 6]), __float_as_uint(acc[8 * i + 7]));
                 }
-            } else if (EPI == MOE_EPI_BF16) {
+            } else if (EPI == MOE_EPI_BF16 || EPI == MOE_EPI_BF16_F32_LAST) {
                 if (valid) {
                     uint16_t* dst = static_cast<uint16_t*>(p.out) + row * p.N + nt * BN + half * 128;
 #pragma unroll
@@ -311,7 +317,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float gte = acc[c];
-                    const float h = gte * __frcp_rn(1.0f + __expf(-gte)) * acc[64 + c];
+                    const float h = __fdividef(gte * acc[64 + c], 1.0f + __expf(-gte));
                     acc[c] = h;
                     amax = fmaxf(amax, fabsf(h));
                 }
@@ -321,23 +327,26 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 if (!mbar_wait(&s.pair[q], tcount & 1u, abort, kWaitLimitNs)) break;
                 amax = fmaxf(amax, s.amax_x[tcount & 1u][ew ^ 4][lane]);
                 const float sc = __fdiv_rn(amax, kE4M3Max);
+                // h is multiplied by the correctly rounded reciprocal of the scale
+                // (one rounding more than the quotient, enough for an E4M3 code)
+                const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
                 if (valid) {
                     const int I = p.N / 2;
                     uint8_t* dst = static_cast<uint8_t*>(p.out) + row * I + nt * 128 + half * 64;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         uint4 w;
-                        w.x = e4m3x4(quant_ratio(acc[16 * i + 0], sc), quant_ratio(acc[16 * i + 1], sc),
-                                     quant_ratio(acc[16 * i + 2], sc), quant_ratio(acc[16 * i + 3], sc));
-                        w.y = e4m3x4(quant_ratio(acc[16 * i + 4], sc), quant_ratio(acc[16 * i + 5], sc),
-                                     quant_ratio(acc[16 * i + 6], sc), quant_ratio(acc[16 * i + 7], sc));
-                        w.z = e4m3x4(quant_ratio(acc[16 * i + 8], sc), quant_ratio(acc[16 * i + 9], sc),
-                                     quant_ratio(acc[16 * i + 10], sc), quant_ratio(acc[16 * i + 11], sc));
-                        w.w = e4m3x4(quant_ratio(acc[16 * i + 12], sc), quant_ratio(acc[16 * i + 13], sc),
-                                     quant_ratio(acc[16 * i + 14], sc), quant_ratio(acc[16 * i + 15], sc));
+                        w.x = e4m3x4(rs * acc[16 * i + 0], rs * acc[16 * i + 1],
+                                     rs * acc[16 * i + 2], rs * acc[16 * i + 3]);
+                        w.y = e4m3x4(rs * acc[16 * i + 4], rs * acc[16 * i + 5],
+                                     rs * acc[16 * i + 6], rs * acc[16 * i + 7]);
+                        w.z = e4m3x4(rs * acc[16 * i + 8], rs * acc[16 * i + 9],
+                                     rs * acc[16 * i + 10], rs * acc[16 * i + 11]);
+                        w.w = e4m3x4(rs * acc[16 * i + 12], rs * acc[16 * i + 13],
+                                     rs * acc[16 * i + 14], rs * acc[16 * i + 15]);
                         reinterpret_cast<uint4*>(dst)[i] = w;
                     }
-                    if (half == 0) p.out_scale[row * (I / 128) + nt] = sc;
+                    if (half == 0) p.out_aux[row * (I / 128) + nt] = sc;
                 }
             }
         }

@@ -7,8 +7,9 @@ namespace moe {
 
 // y[t] = shared[t] + sum_k gate[t][k] * routed[row_of[t][k]] (+ residual[t]),
 // FP32 accumulation in that order, bf16 result (《DeepSeek-V3 Technical
-// Report》深度解读报告 §2.2). One CTA per token, 4 FP32 (16 bytes) per step.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ routed, const float* __restrict__ shared,
+// Report》深度解读报告 §2.2). Routed outputs bf16, shared output FP32. One CTA
+// per token, 4 columns (8 bytes bf16 / 16 bytes FP32) per step.
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ routed, const float* __restrict__ shared,
                                                       const int32_t* __restrict__ row_of, const float* __restrict__ gate,
                                                       const uint16_t* __restrict__ residual, int T, int K, int d,
                                                       uint16_t* __restrict__ y) {
@@ -29,9 +30,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         float4 acc = __ldg(reinterpret_cast<const float4*>(shared + static_cast<int64_t>(t) * d) + v);
         for (int k = 0; k < K; ++k) {
             const float g = gates[k];
-            const float4 u = __ldg(reinterpret_cast<const float4*>(routed + static_cast<int64_t>(rows[k]) * d) + v);
-            acc.x = fmaf(g, u.x, acc.x); acc.y = fmaf(g, u.y, acc.y);
-            acc.z = fmaf(g, u.z, acc.z); acc.w = fmaf(g, u.w, acc.w);
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(routed + static_cast<int64_t>(rows[k]) * d) + v);
+            acc.x = fmaf(g, bf16_lo(u.x), acc.x); acc.y = fmaf(g, bf16_hi(u.x), acc.y);
+            acc.z = fmaf(g, bf16_lo(u.y), acc.z); acc.w = fmaf(g, bf16_hi(u.y), acc.w);
         }
         if (residual != nullptr) {
             const uint2 u = __ldg(reinterpret_cast<const uint2*>(residual + static_cast<int64_t>(t) * d) + v);

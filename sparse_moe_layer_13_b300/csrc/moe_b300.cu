@@ -398,11 +398,14 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, c
 
 moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,
                                 const uint8_t* A, const float* sa, const uint8_t* B, const float* sb, int32_t epilogue,
-                                void* out, float* out_scale, void* stream) {
+                                void* out, float* out_aux, void* stream) {
     if (!offsets || !A || !sa || !B || !sb || !out || rows < 0 || groups < 1 || N < 0 || Kdim < 0)
         return MOE_ERR_INVALID_ARG;
-    if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8 && epilogue != MOE_EPI_F32) return MOE_ERR_INVALID_ARG;
-    if (epilogue == MOE_EPI_SWIGLU_FP8 && !out_scale) return MOE_ERR_INVALID_ARG;
+    if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8 && epilogue != MOE_EPI_F32 &&
+        epilogue != MOE_EPI_BF16_F32_LAST)
+        return MOE_ERR_INVALID_ARG;
+    if ((epilogue == MOE_EPI_SWIGLU_FP8 || epilogue == MOE_EPI_BF16_F32_LAST) && !out_aux) return MOE_ERR_INVALID_ARG;
+    if (epilogue == MOE_EPI_BF16_F32_LAST && !aligned16(out_aux)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
     if (groups > gemm::MAX_GROUPS || N % gemm::BN || N == 0 || Kdim % gemm::BK || Kdim == 0 || rows >= INT32_MAX)
         return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -412,15 +415,16 @@ moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t 
     if (!make_map_u8(&ta, A, static_cast<uint64_t>(Kdim), static_cast<uint64_t>(rows), gemm::BM)) return MOE_ERR_CUDA;
     if (!make_map_u8(&tb, B, static_cast<uint64_t>(Kdim), static_cast<uint64_t>(groups) * N, gemm::BN))
         return MOE_ERR_CUDA;
-    gemm::Params p{offsets, groups, rows, N, Kdim, sa, sb, out, out_scale};
+    gemm::Params p{offsets, groups, rows, N, Kdim, sa, sb, out, out_aux};
     const int64_t tiles_max = (ceil_div(rows, gemm::BM) + groups) * (N / gemm::BN);
     cudaStream_t st = as_stream(stream);
     if (epilogue == MOE_EPI_BF16) return launch_gemm<MOE_EPI_BF16>(ta, tb, p, tiles_max, st);
     if (epilogue == MOE_EPI_F32) return launch_gemm<MOE_EPI_F32>(ta, tb, p, tiles_max, st);
+    if (epilogue == MOE_EPI_BF16_F32_LAST) return launch_gemm<MOE_EPI_BF16_F32_LAST>(ta, tb, p, tiles_max, st);
     return launch_gemm<MOE_EPI_SWIGLU_FP8>(ta, tb, p, tiles_max, st);
 }
 
-moe_status moe_combine(const moe_config* cfg, const float* routed_out, const float* shared_out,
+moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const float* shared_out,
                        const int32_t* row_of, const float* topk_gate, const uint16_t* residual, uint16_t* y,
                        void* stream) {
     const moe_status cs = check_config(cfg);

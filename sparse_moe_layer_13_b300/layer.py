@@ -70,7 +70,8 @@ class MoELayer:
         }
         self.hq = z(R, I, dt=torch.uint8)
         self.hs = z(R, I // 128, dt=torch.float32)
-        self.out = z(R, d, dt=torch.float32)
+        self.out = z(R, d, dt=torch.bfloat16)          # routed rows (the shared rows stay unused)
+        self.out_shared = z(T, d, dt=torch.float32)
         self.y = z(T, d, dt=torch.bfloat16)
 
     def forward(self, x: torch.Tensor, residual: bool = False, update_bias: bool = True,
@@ -95,11 +96,12 @@ class MoELayer:
             ev["gemm1"][1].record()
         if "gemm2" in ev:
             ev["gemm2"][0].record()
-        B.grouped_gemm_fp8(self.perm["offsets"], self.hq, self.hs, self.w.q2, self.w.s2, B.MOE_EPI_F32, self.out)
+        B.grouped_gemm_fp8(self.perm["offsets"], self.hq, self.hs, self.w.q2, self.w.s2, B.MOE_EPI_BF16_F32_LAST,
+                           self.out, self.out_shared)
         if "gemm2" in ev:
             ev["gemm2"][1].record()
         TK = c.T * c.K
-        B.combine(c, self.out[:TK], self.out[TK:], self.perm["row_of"], self.gate, x if residual else None, self.y)
+        B.combine(c, self.out[:TK], self.out_shared, self.perm["row_of"], self.gate, x if residual else None, self.y)
         if update_bias:
             if counts_hook is not None:
                 counts_hook(self.counts)

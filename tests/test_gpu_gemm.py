@@ -43,28 +43,41 @@ SIZES = [
 @gpu
 @pytest.mark.parametrize("case", range(len(SIZES)))
 @pytest.mark.parametrize("N,K", [(256, 128), (512, 384), (768, 1024)])
-@pytest.mark.parametrize("epi", ["bf16", "f32"])
+@pytest.mark.parametrize("epi", ["bf16", "f32", "bf16_f32_last"])
 def test_gemm_plain_epilogues(case, N, K, epi):
     require_gpu()
     from sparse_moe_layer_13_b300 import binding
     offsets, A, sa, B, sb = _problem(SIZES[case], N, K, seed=case * 100 + N + K, trailing=70)
     o_d, A_d, sa_d, B_d, sb_d = _cuda(offsets, A, sa, B, sb)
-    dt, code = (torch.bfloat16, binding.MOE_EPI_BF16) if epi == "bf16" else (torch.float32, binding.MOE_EPI_F32)
+    code = {"bf16": binding.MOE_EPI_BF16, "f32": binding.MOE_EPI_F32,
+            "bf16_f32_last": binding.MOE_EPI_BF16_F32_LAST}[epi]
+    dt = torch.float32 if epi == "f32" else torch.bfloat16
     out = torch.full((A.shape[0], N), -7.0, dtype=dt, device="cuda")
-    binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, code, out)
+    G = len(offsets) - 1
+    last = torch.full((int(offsets[G] - offsets[G - 1]), N), -7.0, dtype=torch.float32, device="cuda")
+    binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, code, out, last if epi == "bf16_f32_last" else None)
     binding.check_device_status()
     got = to_np(out).astype(np.float64)
     absA, absB = A & 0x7F, B & 0x7F
-    for g in range(len(offsets) - 1):
+    for g in range(G):
         r0, r1 = offsets[g], offsets[g + 1]
         if r1 == r0:
             continue
         exact = gemm_fp8(A[r0:r1], sa[r0:r1], B[g], sb[g])
         mag = gemm_fp8(absA[r0:r1], sa[r0:r1], absB[g], sb[g])   # sum of |products|: the FP32 error scale
-        err = np.abs(got[r0:r1] - exact)
-        if epi == "bf16":
+        kind = epi
+        rows_got = got[r0:r1]
+        if epi == "bf16_f32_last":
+            if g == G - 1:
+                kind = "f32"
+                rows_got = to_np(last).astype(np.float64)
+                assert np.all(got[r0:r1] == -7.0)          # the last group goes only to the FP32 output
+            else:
+                kind = "bf16"
+        err = np.abs(rows_got - exact)
+        if kind == "bf16":
             assert np.all(err <= 2.0 ** -8 * np.abs(exact) + 1e-5 * mag + 1e-30), f"group {g}"
-            assert np.mean(got[r0:r1] == round_bf16(exact)) > 0.99
+            assert np.mean(rows_got == round_bf16(exact)) > 0.99
         else:
             assert np.all(err <= 1e-5 * mag + 1e-30), f"group {g}: {(err / mag).max():.3e}"
     assert np.all(got[offsets[-1]:] == -7.0)       # rows outside every group untouched
