@@ -122,7 +122,11 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     cfg = {**CONFIGS, **PROFILE_CONFIGS}[args.config]
-    layer = MoELayer(cfg, dev)
+    offset = inputs.gen_logit_offset(cfg, cfg.zipf_c, dev) if cfg.zipf_s else None
+    layer = MoELayer(cfg, dev, logit_offset=offset)
+    skew = None
+    if cfg.skew_steps:
+        skew = balancing_loop(cfg, layer, dev, binding, inputs, dp)
     # each rank its own tokens: a different x batch per rank
     x = inputs.gen_x(cfg, dev, step=rank)
     hook = dp.allreduce_load if ws > 1 else None
@@ -192,6 +196,23 @@ def run_ours(args):
     fp8_peak = 2.0 * bf16          # E4M3 dense rate is twice bf16 (4.5 vs 2.25 PFLOP/s nominal)
     g1_tflops = f1 / (g1 * 1e-3) / 1e12
     g2_tflops = f2 / (g2 * 1e-3) / 1e12
+    # weight bytes the gate/up GEMM must stream: every expert that received a token, plus the shared one
+    touched = int((layer.counts > 0).sum().item()) + 1
+    w13_bytes = touched * (2 * cfg.I * cfg.d + 4 * (2 * cfg.I // 128) * (cfg.d // 128))
+    a_bytes = cfg.rows * (cfg.d + 4 * cfg.d // 128) + cfg.rows * (cfg.I + 4 * cfg.I // 128)
+    g1_gbs = (w13_bytes + a_bytes) / (g1 * 1e-3) / 1e9
+    weight_bound = cfg.T <= 1024     # a few rows per expert: the GEMMs stream weights
+    if weight_bound:
+        roof = {"kernel": "grouped_gemm_fp8 gate/up + SwiGLU (streams the touched experts' W13)",
+                "bound": "hbm", "achieved": round(g1_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(g1_gbs / hbm, 4), "traffic": None,
+                "algorithmic_bytes": w13_bytes + a_bytes, "touched_experts": touched,
+                "peak_source": f"{src}: HBM copy bandwidth"}
+    else:
+        roof = {"kernel": "grouped_gemm_fp8 gate/up + SwiGLU (largest share of the step)",
+                "bound": "tensor", "achieved": round(g1_tflops, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(g1_tflops / fp8_peak, 4), "traffic": None,
+                "peak_source": f"{src}: bf16 burst {bf16} TFLOP/s x 2 (E4M3/bf16 nominal ratio)"}
     tokens = cfg.T * ws
     value = tokens / (ms * 1e-3)
     out = {
@@ -205,14 +226,13 @@ def run_ours(args):
         "layer_tflops": round(cfg.flops() * ws / (ms * 1e-3) / 1e12, 1),
         "gemm": {"gate_up_swiglu_ms": round(g1, 4), "gate_up_tflops": round(g1_tflops, 1),
                  "down_ms": round(g2, 4), "down_tflops": round(g2_tflops, 1),
-                 "grouped_gemm_tflops": round((f1 + f2) / ((g1 + g2) * 1e-3) / 1e12, 1)},
-        "roofline": {"kernel": "grouped_gemm_fp8 gate/up + SwiGLU (largest share of the step)",
-                     "bound": "tensor", "achieved": round(g1_tflops, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(g1_tflops / fp8_peak, 4), "traffic": None,
-                     "peak_source": f"{src}: bf16 burst {bf16} TFLOP/s x 2 (E4M3/bf16 nominal ratio)"},
+                 "grouped_gemm_tflops": round((f1 + f2) / ((g1 + g2) * 1e-3) / 1e12, 1),
+                 "gate_up_gbs": round(g1_gbs, 1)},
+        "roofline": roof,
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2},
         "gpu_launches": K * layer.LAUNCHES_PER_FORWARD,
+        **({"skew": skew} if skew else {}),
         "clocks": clocks.summary(),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -221,6 +241,26 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def balancing_loop(cfg, layer, dev, binding, inputs, dp):
+    """cfg.skew_steps steps of (route with loads -> end-of-step bias update) on fresh
+    batches; returns the max/mean and min/mean expert load seen at each step."""
+    import torch
+    mx, mn = [], []
+    T_all = dp.global_tokens(cfg.T)
+    for step in range(cfg.skew_steps):
+        x = inputs.gen_x(cfg, dev, step=1000 + step)
+        binding.route(cfg, x, layer.Wr, layer.bias, layer.logit_offset, layer.ws, layer.idx, layer.gate, layer.counts)
+        dp.allreduce_load(layer.counts)
+        binding.bias_update(cfg.E, T_all, cfg.K, layer.counts, cfg.gamma, layer.bias)
+        c = layer.counts.cpu().numpy().astype("float64")
+        mean = T_all * cfg.K / cfg.E
+        mx.append(round(float(c.max() / mean), 3))
+        mn.append(round(float(c.min() / mean), 3))
+    torch.cuda.synchronize()
+    return {"steps": cfg.skew_steps, "gamma": cfg.gamma, "zipf_s": cfg.zipf_s, "zipf_c": cfg.zipf_c,
+            "max_over_mean": mx, "min_over_mean": mn}
 
 
 def cpu_baseline(cfg, n_tokens: int, steps: int):

@@ -32,6 +32,7 @@ class MoEConfig:
     skew_steps: int = 0             # > 0: route + bias update loop length
     gamma: float = 1e-3             # bias update speed
     zipf_s: Optional[float] = None  # per-expert router logit offsets when set
+    zipf_c: float = 0.0             # scale of those offsets
 
     @property
     def rows(self) -> int:
@@ -62,8 +63,10 @@ TINY = MoEConfig("tiny", T=256, d=256, E=16, I=128, K=4, G=4, M=2, gk=2, seed=0,
 MID = MoEConfig("mid", T=4096, d=2048, E=64, I=1408, K=6, G=8, M=3, gk=2, seed=1)
 FULL = MoEConfig("full", T=16384, d=7168, E=256, I=2048, K=8, G=8, M=4, gk=2, seed=2)
 DECODE = MoEConfig("decode", T=128, d=7168, E=256, I=2048, K=8, G=8, M=4, gk=2, seed=3)
+# c = 0.274886: bisection with the FP64 reference router on a seeded 8192-token
+# batch for a hottest-expert load of 8x the mean at step 0 (tests/golden/calibrate_skew.py)
 SKEW = MoEConfig("skew", T=65536, d=7168, E=256, I=2048, K=8, G=8, M=4, gk=2, seed=4,
-                 skew_steps=50, gamma=1e-3, zipf_s=1.1)
+                 skew_steps=50, gamma=1e-3, zipf_s=1.1, zipf_c=0.274886)
 
 CONFIGS = {c.name: c for c in (TINY, MID, FULL, DECODE, SKEW)}
 
