@@ -75,13 +75,14 @@ class MoELayer:
         self.y = z(T, d, dt=torch.bfloat16)
 
     def forward(self, x: torch.Tensor, residual: bool = False, update_bias: bool = True,
-                gamma: float | None = None, counts_hook=None, events=None) -> torch.Tensor:
+                gamma: float | None = None, counts_hook=None, events=None, out: torch.Tensor | None = None) -> torch.Tensor:
         """One layer forward on the current stream.
 
         counts_hook(counts) runs before the bias update (e.g. an all-reduce of
         the expert load across data-parallel ranks); events, if given, is a
         dict of name -> (start, end) torch.cuda.Event pairs recorded around
-        the two grouped GEMMs ("gemm1", "gemm2").
+        the two grouped GEMMs ("gemm1", "gemm2"); out, if given, receives y
+        (bf16 [T][d]) instead of the layer's own buffer.
         """
         c = self.cfg
         ev = events or {}
@@ -101,12 +102,13 @@ class MoELayer:
         if "gemm2" in ev:
             ev["gemm2"][1].record()
         TK = c.T * c.K
-        B.combine(c, self.out[:TK], self.out_shared, self.perm["row_of"], self.gate, x if residual else None, self.y)
+        y = self.y if out is None else out
+        B.combine(c, self.out[:TK], self.out_shared, self.perm["row_of"], self.gate, x if residual else None, y)
         if update_bias:
             if counts_hook is not None:
                 counts_hook(self.counts)
             B.bias_update(c.E, c.T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
-        return self.y
+        return y
 
     # library kernel launches per forward: route 5 (weight split, logits, selection, histogram,
     # scan), quantise 1, permute 4, grouped GEMMs 2, combine 1, bias update 1
