@@ -3,8 +3,9 @@
 Workload: the full-width prefill layer (T=16384 tokens, d=7168, 256 routed +
 1 shared SwiGLU experts, I=2048, top-8, 8 groups / at most 4 per token),
 synthetic seeded inputs and random-init weights. A step is one whole layer
-forward: route -> quantise -> permute -> grouped FP8 GEMM (gate/up, SwiGLU,
-requantise) -> grouped FP8 GEMM (down) -> combine -> bias update.
+forward: route -> permute -> quantise into grouped rows -> grouped FP8 GEMM
+(gate/up, SwiGLU, requantise) -> grouped FP8 GEMM (down) -> combine -> bias
+update.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config full]
   python bench.py --impl reference ...   # the FP64 CPU oracle on a token sample
@@ -218,7 +219,7 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2},
-        "gpu_launches": K * layer.LAUNCHES_PER_FORWARD,
+        "gpu_launches": K * layer.launches_per_forward,
         **({"skew": skew} if skew else {}),
         "clocks": clocks.summary(),
     }

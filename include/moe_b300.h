@@ -127,6 +127,18 @@ moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr,
 moe_status moe_quant_fp8_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                                uint8_t* q, float* scale, void* stream);
 
+/* moe_quant_fp8_1x128 of the T tokens x [T][d] (bf16, contiguous), with
+ * each token's codes and scales written straight into grouped order: to
+ * rows row_of[t][0..K) (as returned by moe_permute) and to the shared
+ * expert's row T*K + t. Same values as moe_quant_fp8_1x128 followed by the
+ * row gather of moe_permute, without the unpermuted copy.
+ *   row_of   device i32 [T][K], values in [0, T*K) (else MOE_ERR_DEVICE_CHECK
+ *            and that copy is not written)
+ *   xq_perm  device u8  [T*K + T][d] out
+ *   xs_perm  device f32 [T*K + T][d/128] out */
+moe_status moe_quant_fp8_1x128_scatter(const moe_config* cfg, const uint16_t* x, const int32_t* row_of,
+                                       uint8_t* xq_perm, float* xs_perm, void* stream);
+
 /* Weight quantisation per 128x128 block, same rule as above with amax over
  * the block (same page, same item). Set-up only; `batch` independent
  * matrices stored back to back.
@@ -158,10 +170,12 @@ moe_status moe_pack_w13(const uint8_t* q1, const float* s1, const uint8_t* q3, c
  *   offsets      device i32 [E+2] out: group g holds rows [offsets[g], offsets[g+1]);
  *                group E is the shared expert (offsets[E] = T*K, offsets[E+1] = T*K + T)
  *   counts       device i32 [E] out or NULL: histogram of topk_idx
- *   sorted_token device i32 [T*K] out: token of each routed row
+ *   sorted_token device i32 [T*K + T] out: token of each grouped row (the
+ *                shared expert's rows T*K + t hold t)
  *   row_of       device i32 [T][K] out: grouped row of each (token, slot)
- *   xq_perm      device u8  [T*K + T][d] out
- *   xs_perm      device f32 [T*K + T][d/128] out
+ *   xq_perm      device u8  [T*K + T][d] out, or NULL together with xs_perm to
+ *                skip the row gather (xq, xs are then not read)
+ *   xs_perm      device f32 [T*K + T][d/128] out or NULL
  *   workspace    device, >= moe_workspace_size(cfg) bytes */
 moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx,
                        const uint8_t* xq, const float* xs,
@@ -219,6 +233,20 @@ moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t 
                                 const uint8_t* A, const float* sa,
                                 const uint8_t* B, const float* sb,
                                 int32_t epilogue, void* out, float* out_aux, void* stream);
+
+/* moe_grouped_gemm_fp8 with the A operand gathered by row: grouped row r
+ * reads row row_index[r] of A [a_rows][Kdim] and of sa [a_rows][Kdim/128]
+ * (TMA gather, four rows per copy), e.g. the unpermuted quantised tokens with
+ * row_index = sorted_token of moe_permute, so the permuted copy of the
+ * activations never has to be written. row_index: device i32 [rows], values
+ * in [0, a_rows) (else MOE_ERR_DEVICE_CHECK and row 0 is read). Other
+ * arguments, layouts and errors as moe_grouped_gemm_fp8. */
+moe_status moe_grouped_gemm_fp8_gather(int32_t groups, const int32_t* offsets, int64_t rows,
+                                       int32_t N, int32_t Kdim,
+                                       const uint8_t* A, const float* sa, int64_t a_rows,
+                                       const int32_t* row_index,
+                                       const uint8_t* B, const float* sb,
+                                       int32_t epilogue, void* out, float* out_aux, void* stream);
 
 /* Gate-weighted un-permute and combine (《DeepSeek-V3 Technical Report》深度解读报告
  * §2.2): y[t] = shared_out[t] + sum_k topk_gate[t][k] * routed_out[row_of[t][k]]

@@ -43,6 +43,9 @@ _SIG = {
     "moe_permute": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_permute_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_gemm_fp8": (ctypes.c_int, [_I32, _P, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P]),
+    "moe_grouped_gemm_fp8_gather": (ctypes.c_int, [_I32, _P, _I64, _I32, _I32, _P, _P, _I64, _P, _P, _P, _I32, _P, _P,
+                                                   _P]),
+    "moe_quant_fp8_1x128_scatter": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_bias_update": (ctypes.c_int, [_I32, _I32, _I32, _P, ctypes.c_float, _P, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
@@ -150,6 +153,21 @@ def quant_1x128(x, q=None, scale=None):
     return q, scale
 
 
+def quant_1x128_scatter(cfg, x, row_of, xq_perm=None, xs_perm=None):
+    """Quantise tokens x [T][d] straight into grouped rows: row_of[t][k] and T*K + t."""
+    _need(x, torch.bfloat16, "x", (cfg.T, cfg.d))
+    _need(row_of, torch.int32, "row_of", (cfg.T, cfg.K))
+    rows = cfg.rows
+    xq_perm = torch.empty(rows, cfg.d, dtype=torch.uint8, device=x.device) if xq_perm is None else xq_perm
+    xs_perm = torch.empty(rows, cfg.d // 128, dtype=torch.float32, device=x.device) if xs_perm is None else xs_perm
+    _need(xq_perm, torch.uint8, "xq_perm", (rows, cfg.d))
+    _need(xs_perm, torch.float32, "xs_perm", (rows, cfg.d // 128))
+    c = config_c(cfg)
+    _call("moe_quant_fp8_1x128_scatter", ctypes.byref(c), _ptr(x), _ptr(row_of), _ptr(xq_perm), _ptr(xs_perm),
+          _stream())
+    return xq_perm, xs_perm
+
+
 def quant_128x128(w, q=None, scale=None):
     """w float32 [rows][cols] or [batch][rows][cols]."""
     _need(w, torch.float32, "w")
@@ -171,27 +189,32 @@ def pack_w13(q1, s1, q3, s3, q13=None, s13=None):
     return q13, s13
 
 
-def permute(cfg, idx, xq, xs, workspace=None, out=None, want_counts=False):
+def permute(cfg, idx, xq=None, xs=None, workspace=None, out=None, want_counts=False, gather_rows=True):
+    """Grouped row order of the (token, expert) pairs; with gather_rows also the
+    grouped copy of the quantised tokens xq, xs (otherwise they may be None)."""
     dev = idx.device
     _need(idx, torch.int32, "topk_idx", (cfg.T, cfg.K))
-    _need(xq, torch.uint8, "xq", (cfg.T, cfg.d))
-    _need(xs, torch.float32, "xs", (cfg.T, cfg.d // 128))
+    if gather_rows:
+        _need(xq, torch.uint8, "xq", (cfg.T, cfg.d))
+        _need(xs, torch.float32, "xs", (cfg.T, cfg.d // 128))
+    else:
+        xq = xs = None
     rows = cfg.rows
     if out is None:
         out = {
             "offsets": torch.empty(cfg.E + 2, dtype=torch.int32, device=dev),
             "counts": torch.empty(cfg.E, dtype=torch.int32, device=dev) if want_counts else None,
-            "sorted_token": torch.empty(cfg.T * cfg.K, dtype=torch.int32, device=dev),
+            "sorted_token": torch.empty(cfg.T * cfg.K + cfg.T, dtype=torch.int32, device=dev),
             "row_of": torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev),
-            "xq_perm": torch.empty(rows, cfg.d, dtype=torch.uint8, device=dev),
-            "xs_perm": torch.empty(rows, cfg.d // 128, dtype=torch.float32, device=dev),
+            "xq_perm": torch.empty(rows, cfg.d, dtype=torch.uint8, device=dev) if gather_rows else None,
+            "xs_perm": torch.empty(rows, cfg.d // 128, dtype=torch.float32, device=dev) if gather_rows else None,
         }
     if workspace is None:
         workspace = torch.empty(workspace_size(cfg), dtype=torch.uint8, device=dev)
     c = config_c(cfg)
     _call("moe_permute", ctypes.byref(c), _ptr(idx), _ptr(xq), _ptr(xs), _ptr(out["offsets"]), _ptr(out["counts"]),
-          _ptr(out["sorted_token"]), _ptr(out["row_of"]), _ptr(out["xq_perm"]), _ptr(out["xs_perm"]),
-          _ptr(workspace), workspace.numel(), _stream())
+          _ptr(out["sorted_token"]), _ptr(out["row_of"]), _ptr(out["xq_perm"] if gather_rows else None),
+          _ptr(out["xs_perm"] if gather_rows else None), _ptr(workspace), workspace.numel(), _stream())
     return out
 
 
@@ -210,7 +233,7 @@ def permute_noalloc(cfg, idx, xq, xs, out=None, want_counts=False):
         out = {
             "offsets": torch.empty(cfg.E + 2, dtype=torch.int32, device=dev),
             "counts": torch.empty(cfg.E, dtype=torch.int32, device=dev) if want_counts else None,
-            "sorted_token": torch.empty(cfg.T * cfg.K, dtype=torch.int32, device=dev),
+            "sorted_token": torch.empty(cfg.T * cfg.K + cfg.T, dtype=torch.int32, device=dev),
             "row_of": torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev),
             "xq_perm": torch.empty(rows, cfg.d, dtype=torch.uint8, device=dev),
             "xs_perm": torch.empty(rows, cfg.d // 128, dtype=torch.float32, device=dev),
@@ -222,18 +245,22 @@ def permute_noalloc(cfg, idx, xq, xs, out=None, want_counts=False):
     return out
 
 
-def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out_scale=None, last_rows=None):
+def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out_scale=None, last_rows=None,
+                     row_index=None):
     """offsets i32 [G+1]; A u8 [rows][K]; sa f32 [rows][K/128]; B u8 [G][N][K]; sb f32 [G][N/128][K/128].
 
     out_scale is the auxiliary output: h scales for the SwiGLU epilogue, or
     the FP32 output of the last group (last_rows rows) for MOE_EPI_BF16_F32_LAST.
     """
     groups = offsets.numel() - 1
-    rows, Kdim = A.shape
+    a_rows, Kdim = A.shape
+    rows = a_rows if row_index is None else row_index.numel()
     N = B.shape[1]
     _need(offsets, torch.int32, "offsets")
     _need(A, torch.uint8, "A")
-    _need(sa, torch.float32, "sa", (rows, Kdim // 128))
+    _need(sa, torch.float32, "sa", (a_rows, Kdim // 128))
+    if row_index is not None:
+        _need(row_index, torch.int32, "row_index")
     _need(B, torch.uint8, "B", (groups, N, Kdim))
     _need(sb, torch.float32, "sb", (groups, N // 128, Kdim // 128))
     if epilogue == MOE_EPI_BF16:
@@ -248,8 +275,12 @@ def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out
         out = torch.empty(rows, N // 2, dtype=torch.uint8, device=A.device) if out is None else out
         out_scale = (torch.empty(rows, N // 256, dtype=torch.float32, device=A.device)
                      if out_scale is None else out_scale)
-    _call("moe_grouped_gemm_fp8", groups, _ptr(offsets), rows, N, Kdim, _ptr(A), _ptr(sa), _ptr(B), _ptr(sb),
-          epilogue, _ptr(out), _ptr(out_scale), _stream())
+    if row_index is None:
+        _call("moe_grouped_gemm_fp8", groups, _ptr(offsets), rows, N, Kdim, _ptr(A), _ptr(sa), _ptr(B), _ptr(sb),
+              epilogue, _ptr(out), _ptr(out_scale), _stream())
+    else:
+        _call("moe_grouped_gemm_fp8_gather", groups, _ptr(offsets), rows, N, Kdim, _ptr(A), _ptr(sa), a_rows,
+              _ptr(row_index), _ptr(B), _ptr(sb), epilogue, _ptr(out), _ptr(out_scale), _stream())
     return out, out_scale
 
 

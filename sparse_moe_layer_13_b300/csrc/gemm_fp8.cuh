@@ -35,6 +35,7 @@ constexpr int BN = 256;
 constexpr int BK = 128;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
+static_assert(BM == 32 * 4, "gather mode: one gather4 (four rows) per producer lane");
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 384;
@@ -77,6 +78,8 @@ struct Params {
     const float* sb;
     void* out;
     float* out_aux;      // SwiGLU: h scales; BF16_F32_LAST: FP32 output of the last group
+    const int32_t* row_index;   // gather mode: grouped row r reads A and sa row row_index[r]
+    int64_t a_rows;             // gather mode: rows of A
 };
 
 // tile -> (group, row tile inside the group, column tile)
@@ -92,7 +95,9 @@ __device__ __forceinline__ void decode_tile(const Smem& s, int groups, int ntile
     mt = mtg - s.mtile_prefix[g];
 }
 
-template <int EPI>
+// GATHER: A rows are fetched by index (TMA gather4, four rows per copy)
+// instead of as one 128-row tile.
+template <int EPI, bool GATHER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -162,27 +167,49 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
       if (warp == 0) {
         // ---------------------------------------------------- TMA producer ----
-        if (lane == 0) {
-            uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
-                int g, mt, nt;
-                decode_tile(s, groups, ntiles, tile, g, mt, nt);
-                const int row0 = s.row_start[g] + mt * BM;
-                const int brow = g * p.N + nt * BN;
-                for (int kc = 0; kc < nkc; ++kc, ++it) {
-                    const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(&s.empty[st], ph ^ 1u, abort, kWaitLimitNs)) break;
-                    mbar_expect_tx(&s.full[st], STAGE_BYTES);
-                    tma_load_2d(sA + st * A_BYTES, &tmA, &s.full[st], kc * BK, row0);
-                    tma_load_2d(sB + st * B_BYTES, &tmB, &s.full[st], kc * BK, brow);
+        // Lane 0 waits for a free stage and arms its barrier; in gather mode
+        // every lane then issues one gather4 (rows 4*lane .. 4*lane+3 of the
+        // tile, indices held in registers for the whole tile).
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            int g, mt, nt;
+            decode_tile(s, groups, ntiles, tile, g, mt, nt);
+            const int row0 = s.row_start[g] + mt * BM;
+            const int brow = g * p.N + nt * BN;
+            int src[4] = {0, 0, 0, 0};
+            if (GATHER) {
+                // rows past the group's end read row 0 (their results are dropped)
+                const int end = s.row_start[g + 1];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int r = row0 + 4 * static_cast<int>(lane) + q;
+                    int v = r < end ? __ldg(p.row_index + r) : 0;
+                    if (v < 0 || v >= p.a_rows) { set_status(MOE_ERR_DEVICE_CHECK); v = 0; }
+                    src[q] = v;
                 }
             }
-            if (*abort) {
-                // let every issued copy land before the CTA exits
-                const uint32_t first = it > STAGES ? it - STAGES : 0;
-                for (uint32_t j = first; j < it; ++j)
-                    mbar_wait(&s.full[j % STAGES], (j / STAGES) & 1u, nullptr, kWaitLimitNs);
+            for (int kc = 0; kc < nkc; ++kc, ++it) {
+                const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
+                if (lane == 0) {
+                    ok = mbar_wait(&s.empty[st], ph ^ 1u, abort, kWaitLimitNs);
+                    if (ok) mbar_expect_tx(&s.full[st], STAGE_BYTES);
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
+                if (GATHER)
+                    tma_gather4_2d(sA + st * A_BYTES + lane * 4 * BK, &tmA, &s.full[st], kc * BK, src[0], src[1],
+                                   src[2], src[3]);
+                else if (lane == 0)
+                    tma_load_2d(sA + st * A_BYTES, &tmA, &s.full[st], kc * BK, row0);
+                if (lane == 0) tma_load_2d(sB + st * B_BYTES, &tmB, &s.full[st], kc * BK, brow);
             }
+            if (!ok || __shfl_sync(0xffffffffu, *abort, 0)) break;
+        }
+        if (lane == 0 && *abort) {
+            // let every issued copy land before the CTA exits
+            const uint32_t first = it > STAGES ? it - STAGES : 0;
+            for (uint32_t j = first; j < it; ++j)
+                mbar_wait(&s.full[j % STAGES], (j / STAGES) & 1u, nullptr, kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer ----
@@ -226,7 +253,12 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             const int m_valid = s.row_start[g + 1] - s.row_start[g] - mt * BM;
             const bool valid = rit < m_valid;
             const int64_t row = static_cast<int64_t>(s.row_start[g]) + mt * BM + rit;
-            const float* sa_row = p.sa + (valid ? row : 0) * nkc;
+            int64_t src_row = valid ? row : 0;
+            if (GATHER && valid) {
+                src_row = __ldg(p.row_index + row);
+                if (src_row < 0 || src_row >= p.a_rows) src_row = 0;      // reported by the producer
+            }
+            const float* sa_row = p.sa + src_row * nkc;
             // weight scale rows: SwiGLU -> gate block 2*nt, up block 2*nt+1; otherwise block 2*nt+half
             const float* sb0 = p.sb + (static_cast<int64_t>(g) * nbn + 2 * nt + (EPI == MOE_EPI_SWIGLU_FP8 ? 0 : half)) * nkc;
             const float* sb1 = (EPI == MOE_EPI_SWIGLU_FP8) ? sb0 + nkc : sb0;

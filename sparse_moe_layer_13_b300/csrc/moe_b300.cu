@@ -155,19 +155,60 @@ void launch_select(const moe_config* c, const float* z, int ks, const float* off
     else launch_select_e<32>(c, z, ks, off, bias, idx, gate, grid, smem, st);
 }
 
-template <int EPI>
+template <int EPI, bool GATHER>
 moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p, int64_t tiles_max,
                        cudaStream_t st) {
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm::grouped_gemm_fp8_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm::grouped_gemm_fp8_kernel<EPI, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(gemm::SMEM_BYTES)) != cudaSuccess)
             return MOE_ERR_CUDA;
         attr_set = true;
     }
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_max, 1)));
-    gemm::grouped_gemm_fp8_kernel<EPI><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, st>>>(ta, tb, p);
+    gemm::grouped_gemm_fp8_kernel<EPI, GATHER><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, st>>>(ta, tb, p);
     return launch_status();
+}
+
+template <bool GATHER>
+moe_status launch_gemm_epi(int32_t epilogue, const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p,
+                           int64_t tiles_max, cudaStream_t st) {
+    if (epilogue == MOE_EPI_BF16) return launch_gemm<MOE_EPI_BF16, GATHER>(ta, tb, p, tiles_max, st);
+    if (epilogue == MOE_EPI_F32) return launch_gemm<MOE_EPI_F32, GATHER>(ta, tb, p, tiles_max, st);
+    if (epilogue == MOE_EPI_BF16_F32_LAST) return launch_gemm<MOE_EPI_BF16_F32_LAST, GATHER>(ta, tb, p, tiles_max, st);
+    return launch_gemm<MOE_EPI_SWIGLU_FP8, GATHER>(ta, tb, p, tiles_max, st);
+}
+
+// Shared checks and launch of the grouped GEMM; row_index == nullptr: A is in grouped row order.
+moe_status grouped_gemm(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,
+                        const uint8_t* A, const float* sa, int64_t a_rows, const int32_t* row_index,
+                        const uint8_t* B, const float* sb, int32_t epilogue, void* out, float* out_aux,
+                        cudaStream_t st) {
+    if (!offsets || !A || !sa || !B || !sb || !out || rows < 0 || a_rows < 0 || groups < 1 || N < 0 || Kdim < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8 && epilogue != MOE_EPI_F32 &&
+        epilogue != MOE_EPI_BF16_F32_LAST)
+        return MOE_ERR_INVALID_ARG;
+    if ((epilogue == MOE_EPI_SWIGLU_FP8 || epilogue == MOE_EPI_BF16_F32_LAST) && !out_aux) return MOE_ERR_INVALID_ARG;
+    if (epilogue == MOE_EPI_BF16_F32_LAST && !aligned16(out_aux)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if (groups > gemm::MAX_GROUPS || N % gemm::BN || N == 0 || Kdim % gemm::BK || Kdim == 0 || rows >= INT32_MAX ||
+        a_rows >= INT32_MAX)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(groups) * N >= INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (row_index != nullptr && a_rows == 0) return MOE_ERR_INVALID_ARG;
+    CUtensorMap ta, tb;
+    const bool gather = row_index != nullptr;
+    if (!make_map_u8(&ta, A, static_cast<uint64_t>(Kdim), static_cast<uint64_t>(gather ? a_rows : rows),
+                     gather ? 1u : static_cast<uint32_t>(gemm::BM)))
+        return MOE_ERR_CUDA;
+    if (!make_map_u8(&tb, B, static_cast<uint64_t>(Kdim), static_cast<uint64_t>(groups) * N, gemm::BN))
+        return MOE_ERR_CUDA;
+    gemm::Params p{offsets, groups, rows, N, Kdim, sa, sb, out, out_aux, row_index, a_rows};
+    const int64_t tiles_max = (ceil_div(rows, gemm::BM) + groups) * (N / gemm::BN);
+    if (gather) return launch_gemm_epi<true>(epilogue, ta, tb, p, tiles_max, st);
+    return launch_gemm_epi<false>(epilogue, ta, tb, p, tiles_max, st);
 }
 
 const char* kStatusNames[] = {
@@ -295,12 +336,23 @@ moe_status moe_quant_fp8_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
     if (!x || !q || !scale || rows < 0 || cols < 0 || ld < cols) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || ld % 8) return MOE_ERR_INVALID_ARG;
     if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0 || cols == 0) return MOE_OK;
     const int64_t tiles = rows * (cols / 128);
     // 8 warps per CTA, two tiles per warp step, two steps in flight per thread
     const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 32), static_cast<int64_t>(num_sms()) * 16));
-    quant_1x128_kernel<<<grid, 256, 0, as_stream(stream)>>>(x, rows, cols, ld, q, scale);
+    quant_1x128_kernel<false><<<grid, 256, 0, as_stream(stream)>>>(x, rows, cols, ld, q, scale, nullptr, 0);
+    return launch_status();
+}
+
+moe_status moe_quant_fp8_1x128_scatter(const moe_config* cfg, const uint16_t* x, const int32_t* row_of,
+                                       uint8_t* xq_perm, float* xs_perm, void* stream) {
+    if (const moe_status st = check_config(cfg); st != MOE_OK) return st;
+    if (!x || !row_of || !xq_perm || !xs_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq_perm)) return MOE_ERR_INVALID_ARG;
+    const int64_t tiles = static_cast<int64_t>(cfg->T) * (cfg->d / 128);
+    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 32), static_cast<int64_t>(num_sms()) * 16));
+    quant_1x128_kernel<true><<<grid, 256, 0, as_stream(stream)>>>(x, cfg->T, cfg->d, cfg->d, xq_perm, xs_perm,
+                                                                   row_of, cfg->K);
     return launch_status();
 }
 
@@ -336,9 +388,10 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, const uin
                        float* xs_perm, void* workspace, size_t workspace_bytes, void* stream) {
     const moe_status cs = check_config(cfg);
     if (cs != MOE_OK) return cs;
-    if (!topk_idx || !xq || !xs || !offsets || !sorted_token || !row_of || !xq_perm || !xs_perm)
-        return MOE_ERR_INVALID_ARG;
-    if (!aligned16(xq) || !aligned16(xq_perm) || !aligned16(topk_idx)) return MOE_ERR_INVALID_ARG;
+    if (!topk_idx || !offsets || !sorted_token || !row_of) return MOE_ERR_INVALID_ARG;
+    const bool gather_rows = xq_perm != nullptr || xs_perm != nullptr;
+    if (gather_rows && (!xq || !xs || !xq_perm || !xs_perm)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(topk_idx) || (gather_rows && (!aligned16(xq) || !aligned16(xq_perm)))) return MOE_ERR_INVALID_ARG;
     const WsLayout wl = ws_layout(cfg);
     if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);
@@ -355,6 +408,7 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, const uin
     perm::scatter_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E, blk_base, row_of,
                                                                sorted_token);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (!gather_rows) return MOE_OK;
     const int64_t rows = npairs + cfg->T;
     perm::gather_kernel<<<static_cast<unsigned>(ceil_div(rows * 32, 256)), 256, 0, st>>>(
         sorted_token, cfg->T, cfg->K, cfg->d, xq, xs, xq_perm, xs_perm);
@@ -368,9 +422,10 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, c
     if (cs != MOE_OK) return cs;
     const int64_t nblk = ceil_div(cfg->T, perm::kTokPerBlk);
     if (2 * nblk * cfg->E > static_cast<int64_t>(kPermuteScratchInts)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (!topk_idx || !xq || !xs || !offsets || !sorted_token || !row_of || !xq_perm || !xs_perm)
-        return MOE_ERR_INVALID_ARG;
-    if (!aligned16(xq) || !aligned16(xq_perm) || !aligned16(topk_idx)) return MOE_ERR_INVALID_ARG;
+    if (!topk_idx || !offsets || !sorted_token || !row_of) return MOE_ERR_INVALID_ARG;
+    const bool gather_rows = xq_perm != nullptr || xs_perm != nullptr;
+    if (gather_rows && (!xq || !xs || !xq_perm || !xs_perm)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(topk_idx) || (gather_rows && (!aligned16(xq) || !aligned16(xq_perm)))) return MOE_ERR_INVALID_ARG;
     int32_t* scratch = nullptr;
     const moe_status ss = permute_scratch(&scratch);
     if (ss != MOE_OK) return ss;
@@ -390,6 +445,7 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, c
     perm::scatter_kernel<<<static_cast<unsigned>(nblk), perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E,
                                                                                       blk_base, row_of, sorted_token);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (!gather_rows) return MOE_OK;
     const int64_t rows = npairs + cfg->T;
     perm::gather_kernel<<<static_cast<unsigned>(ceil_div(rows * 32, 256)), 256, 0, st>>>(
         sorted_token, cfg->T, cfg->K, cfg->d, xq, xs, xq_perm, xs_perm);
@@ -399,29 +455,17 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, c
 moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,
                                 const uint8_t* A, const float* sa, const uint8_t* B, const float* sb, int32_t epilogue,
                                 void* out, float* out_aux, void* stream) {
-    if (!offsets || !A || !sa || !B || !sb || !out || rows < 0 || groups < 1 || N < 0 || Kdim < 0)
-        return MOE_ERR_INVALID_ARG;
-    if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8 && epilogue != MOE_EPI_F32 &&
-        epilogue != MOE_EPI_BF16_F32_LAST)
-        return MOE_ERR_INVALID_ARG;
-    if ((epilogue == MOE_EPI_SWIGLU_FP8 || epilogue == MOE_EPI_BF16_F32_LAST) && !out_aux) return MOE_ERR_INVALID_ARG;
-    if (epilogue == MOE_EPI_BF16_F32_LAST && !aligned16(out_aux)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-    if (groups > gemm::MAX_GROUPS || N % gemm::BN || N == 0 || Kdim % gemm::BK || Kdim == 0 || rows >= INT32_MAX)
-        return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (static_cast<int64_t>(groups) * N >= INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (rows == 0) return MOE_OK;
-    CUtensorMap ta, tb;
-    if (!make_map_u8(&ta, A, static_cast<uint64_t>(Kdim), static_cast<uint64_t>(rows), gemm::BM)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&tb, B, static_cast<uint64_t>(Kdim), static_cast<uint64_t>(groups) * N, gemm::BN))
-        return MOE_ERR_CUDA;
-    gemm::Params p{offsets, groups, rows, N, Kdim, sa, sb, out, out_aux};
-    const int64_t tiles_max = (ceil_div(rows, gemm::BM) + groups) * (N / gemm::BN);
-    cudaStream_t st = as_stream(stream);
-    if (epilogue == MOE_EPI_BF16) return launch_gemm<MOE_EPI_BF16>(ta, tb, p, tiles_max, st);
-    if (epilogue == MOE_EPI_F32) return launch_gemm<MOE_EPI_F32>(ta, tb, p, tiles_max, st);
-    if (epilogue == MOE_EPI_BF16_F32_LAST) return launch_gemm<MOE_EPI_BF16_F32_LAST>(ta, tb, p, tiles_max, st);
-    return launch_gemm<MOE_EPI_SWIGLU_FP8>(ta, tb, p, tiles_max, st);
+    return grouped_gemm(groups, offsets, rows, N, Kdim, A, sa, rows, nullptr, B, sb, epilogue, out, out_aux,
+                        as_stream(stream));
+}
+
+moe_status moe_grouped_gemm_fp8_gather(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,
+                                       const uint8_t* A, const float* sa, int64_t a_rows, const int32_t* row_index,
+                                       const uint8_t* B, const float* sb, int32_t epilogue, void* out, float* out_aux,
+                                       void* stream) {
+    if (!row_index) return MOE_ERR_INVALID_ARG;
+    return grouped_gemm(groups, offsets, rows, N, Kdim, A, sa, a_rows, row_index, B, sb, epilogue, out, out_aux,
+                        as_stream(stream));
 }
 
 moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const float* shared_out,

@@ -11,7 +11,8 @@
 //  3. scatter_kernel: recomputes the per-warp histograms, turns them into
 //                     per-warp starting rows, then assigns rows in order:
 //                     rank inside a 32-pair batch = popc(same-expert lanes
-//                     below me). Writes row_of and sorted_token.
+//                     below me). Writes row_of and sorted_token (whose tail
+//                     T*K + t holds t, the shared expert's rows).
 //  4. gather_kernel:  one warp per grouped row copies the E4M3 row and its
 //                     1x128 scales (16-byte vectors); shared-expert rows
 //                     T*K + t copy token t.
@@ -135,6 +136,13 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(const int32_t* __r
         }
     }
     __syncthreads();
+    // shared-expert rows T*K + t read token t
+    {
+        const int64_t T = npairs / K;
+        const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokPerBlk;
+        for (int64_t t = t0 + threadIdx.x; t < min(t0 + kTokPerBlk, T); t += blockDim.x)
+            sorted_token[npairs + t] = static_cast<int32_t>(t);
+    }
     int* h = hist + (threadIdx.x >> 5) * E;
     const uint32_t lane = lane_id();
     for (int64_t b = sb; b < se; b += 32) {
@@ -160,8 +168,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
     const int64_t rows = static_cast<int64_t>(T) * K + T;
     const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (r >= rows) return;
-    const int64_t tk = static_cast<int64_t>(T) * K;
-    int src = (r < tk) ? __ldg(sorted_token + r) : static_cast<int>(r - tk);
+    int src = __ldg(sorted_token + r);
     if (src < 0 || src >= T) { set_status(MOE_ERR_DEVICE_CHECK); src = 0; }
     const uint4* s = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(src) * d);
     uint4* dst = reinterpret_cast<uint4*>(xq_perm + r * d);

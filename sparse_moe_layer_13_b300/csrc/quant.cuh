@@ -12,9 +12,16 @@ namespace moe {
 // by shuffles inside the half warp, 8 E4M3 codes per lane (8-byte stores);
 // each warp step covers two tiles and a thread keeps two steps in flight.
 // Grid-stride over tile pairs, so any grid size is valid.
+// SCATTER: row r of x is token r of a routed batch; its codes and scale go
+// to the K grouped rows row_of[r][0..K) and to the shared-expert row
+// rows*K + r of q / scale instead of to row r (K <= 16: lane k of the half
+// warp loads row_of[r][k]). A grouped row outside [0, rows*K) is reported
+// and not written.
+template <bool SCATTER>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                           int64_t cols, int64_t ld, uint8_t* __restrict__ q,
-                                                          float* __restrict__ scale) {
+                                                          float* __restrict__ scale,
+                                                          const int32_t* __restrict__ row_of, int K) {
     const int64_t tiles_per_row = cols / 128;
     const int64_t ntiles = rows * tiles_per_row;
     const int64_t npairs = (ntiles + 1) / 2;
@@ -26,6 +33,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
         uint4 w[2];
         int64_t tile[2];
         bool live[2];
+        int dst[2] = {0, 0};
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             tile[u] = 2 * (p0 + u * nwarps) + (lane >> 4);
@@ -34,6 +42,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
             if (live[u]) {
                 const int64_t r = tile[u] / tiles_per_row, c = tile[u] - r * tiles_per_row;
                 w[u] = __ldg(reinterpret_cast<const uint4*>(x + r * ld + c * 128) + sub);
+                if (SCATTER && static_cast<int>(sub) < K) dst[u] = __ldg(row_of + r * K + sub);
             }
         }
 #pragma unroll
@@ -44,14 +53,29 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
                                fmaxf(fmaxf(fabsf(v4), fabsf(v5)), fmaxf(fabsf(v6), fabsf(v7))));
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            if (!live[u]) continue;
             const float s = __fdiv_rn(amax, kE4M3Max);
-            const int64_t r = tile[u] / tiles_per_row, c = tile[u] - r * tiles_per_row;
             uint2 codes;
             codes.x = e4m3x4(quant_ratio(v0, s), quant_ratio(v1, s), quant_ratio(v2, s), quant_ratio(v3, s));
             codes.y = e4m3x4(quant_ratio(v4, s), quant_ratio(v5, s), quant_ratio(v6, s), quant_ratio(v7, s));
-            reinterpret_cast<uint2*>(q + r * cols + c * 128)[sub] = codes;
-            if (sub == 0) scale[r * tiles_per_row + c] = s;
+            const int64_t r = tile[u] / tiles_per_row, c = tile[u] - r * tiles_per_row;
+            if (!SCATTER) {
+                if (!live[u]) continue;
+                reinterpret_cast<uint2*>(q + r * cols + c * 128)[sub] = codes;
+                if (sub == 0) scale[r * tiles_per_row + c] = s;
+            } else {
+                // every lane of the warp takes part in the shuffles, live or not
+                const int64_t routed = rows * K;
+                for (int k = 0; k <= K; ++k) {
+                    int64_t row = k < K ? __shfl_sync(0xffffffffu, dst[u], (lane & 16) + k) : routed + r;
+                    if (!live[u]) continue;
+                    if (k < K && (row < 0 || row >= routed)) {
+                        if (sub == 0) set_status(MOE_ERR_DEVICE_CHECK);
+                        continue;
+                    }
+                    reinterpret_cast<uint2*>(q + row * cols + c * 128)[sub] = codes;
+                    if (sub == 0) scale[row * tiles_per_row + c] = s;
+                }
+            }
         }
     }
 }

@@ -2,10 +2,19 @@
 
 《DeepSeek-V3 Technical Report》深度解读报告 §2.2-§2.4 and "DeepSeek-V3的MoE架构
 设计革新" §2 describe the layer; this module only owns device buffers and
-calls, in order: moe_route -> moe_quant_fp8_1x128 -> moe_permute ->
+calls, in order: moe_route -> moe_permute (row order only) ->
+moe_quant_fp8_1x128_scatter (tokens quantised straight into grouped rows) ->
 moe_grouped_gemm_fp8 (gate/up + SwiGLU + requantisation) ->
-moe_grouped_gemm_fp8 (down) -> moe_combine -> moe_bias_update.
-Expert E (the last group) is the shared expert.
+moe_grouped_gemm_fp8 (down) -> moe_combine -> moe_bias_update. Expert E (the
+last group) is the shared expert.
+
+token_rows picks how the gate/up GEMM gets its grouped token rows:
+  "scatter"  the quantiser writes them (default, least traffic);
+  "copy"     quantise in token order, then moe_permute gathers a copy;
+  "gather"   quantise in token order and let the GEMM fetch rows by index
+             (moe_grouped_gemm_fp8_gather: no grouped copy, (K+1)*T*d fewer
+             bytes of device memory, slower GEMM).
+All three give bit-identical results.
 """
 from __future__ import annotations
 
@@ -47,8 +56,11 @@ class MoELayer:
     """One layer instance: router weight, selection bias, expert weights, buffers."""
 
     def __init__(self, cfg: MoEConfig, device="cuda", weights: ExpertWeights | None = None,
-                 logit_offset: torch.Tensor | None = None):
+                 logit_offset: torch.Tensor | None = None, token_rows: str = "scatter"):
+        if token_rows not in ("scatter", "copy", "gather"):
+            raise ValueError(f"token_rows: {token_rows!r}")
         self.cfg = cfg
+        self.token_rows = token_rows
         self.device = device
         self.Wr = inputs.gen_router(cfg, device)
         self.bias = inputs.gen_bias(cfg, device)
@@ -61,12 +73,16 @@ class MoELayer:
         self.idx = z(T, K, dt=torch.int32)
         self.gate = z(T, K, dt=torch.float32)
         self.counts = z(E, dt=torch.int32)
-        self.xq = z(T, d, dt=torch.uint8)
-        self.xs = z(T, d // 128, dt=torch.float32)
+        grouped = token_rows != "gather"
+        self.xq = z(T, d, dt=torch.uint8) if token_rows != "scatter" else None
+        self.xs = z(T, d // 128, dt=torch.float32) if token_rows != "scatter" else None
+        self.xq_perm = z(R, d, dt=torch.uint8) if grouped else None
+        self.xs_perm = z(R, d // 128, dt=torch.float32) if grouped else None
         self.perm = {
             "offsets": z(E + 2, dt=torch.int32), "counts": None,
-            "sorted_token": z(T * K, dt=torch.int32), "row_of": z(T, K, dt=torch.int32),
-            "xq_perm": z(R, d, dt=torch.uint8), "xs_perm": z(R, d // 128, dt=torch.float32),
+            "sorted_token": z(R, dt=torch.int32), "row_of": z(T, K, dt=torch.int32),
+            "xq_perm": self.xq_perm if token_rows == "copy" else None,
+            "xs_perm": self.xs_perm if token_rows == "copy" else None,
         }
         self.hq = z(R, I, dt=torch.uint8)
         self.hs = z(R, I // 128, dt=torch.float32)
@@ -87,12 +103,20 @@ class MoELayer:
         c = self.cfg
         ev = events or {}
         B.route(c, x, self.Wr, self.bias, self.logit_offset, self.ws, self.idx, self.gate, self.counts)
-        B.quant_1x128(x, self.xq, self.xs)
-        B.permute(c, self.idx, self.xq, self.xs, self.ws, self.perm)
+        mode = self.token_rows
+        if mode != "scatter":
+            B.quant_1x128(x, self.xq, self.xs)
+        B.permute(c, self.idx, self.xq, self.xs, self.ws, self.perm, gather_rows=mode == "copy")
+        if mode == "scatter":
+            B.quant_1x128_scatter(c, x, self.perm["row_of"], self.xq_perm, self.xs_perm)
         if "gemm1" in ev:
             ev["gemm1"][0].record()
-        B.grouped_gemm_fp8(self.perm["offsets"], self.perm["xq_perm"], self.perm["xs_perm"], self.w.q13, self.w.s13,
-                           B.MOE_EPI_SWIGLU_FP8, self.hq, self.hs)
+        if mode == "gather":
+            B.grouped_gemm_fp8(self.perm["offsets"], self.xq, self.xs, self.w.q13, self.w.s13, B.MOE_EPI_SWIGLU_FP8,
+                               self.hq, self.hs, row_index=self.perm["sorted_token"])
+        else:
+            B.grouped_gemm_fp8(self.perm["offsets"], self.xq_perm, self.xs_perm, self.w.q13, self.w.s13,
+                               B.MOE_EPI_SWIGLU_FP8, self.hq, self.hs)
         if "gemm1" in ev:
             ev["gemm1"][1].record()
         if "gemm2" in ev:
@@ -111,5 +135,8 @@ class MoELayer:
         return y
 
     # library kernel launches per forward: route 5 (weight split, logits, selection, histogram,
-    # scan), quantise 1, permute 4, grouped GEMMs 2, combine 1, bias update 1
-    LAUNCHES_PER_FORWARD = 14
+    # scan), quantise 1, permute 3 (+1 row gather for "copy"), grouped GEMMs 2, combine 1,
+    # bias update 1
+    @property
+    def launches_per_forward(self) -> int:
+        return 13 + int(self.token_rows == "copy")

@@ -125,6 +125,104 @@ def test_gemm_swiglu_epilogue(case, I, K):
     assert np.all(ghq[offsets[-1]:] == 0x55) and np.all(ghs[offsets[-1]:] == -1.0)
 
 
+def _row_index(rng, rows, a_rows):
+    """Grouped row -> A row: a permutation of the A rows, then repeats, as a
+    token-to-expert gather makes (every token read K + 1 times)."""
+    idx = np.concatenate([rng.permutation(a_rows), rng.integers(0, a_rows, max(0, rows - a_rows))])[:rows]
+    return idx.astype(np.int32)
+
+
+@gpu
+@pytest.mark.parametrize("case", range(len(SIZES)))
+@pytest.mark.parametrize("N,K,a_rows", [(256, 128, 7), (512, 384, 1000), (768, 1024, 333)])
+@pytest.mark.parametrize("epi", ["bf16", "f32"])
+def test_gemm_gathered_rows(case, N, K, a_rows, epi):
+    """A rows fetched by index give exactly the GEMM of the gathered matrix."""
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding
+    rng = np.random.default_rng(case * 7 + K)
+    sizes = SIZES[case]
+    G = len(sizes)
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    rows = int(offsets[-1])
+    A = _codes(rng, (a_rows, K))
+    sa = rng.uniform(0.5, 2.0, (a_rows, K // 128)).astype(np.float32) / 448
+    B = _codes(rng, (G, N, K))
+    sb = rng.uniform(0.5, 2.0, (G, N // 128, K // 128)).astype(np.float32) / 448
+    ridx = _row_index(rng, rows, a_rows)
+    o_d, A_d, sa_d, B_d, sb_d, ri_d = _cuda(offsets, A, sa, B, sb, ridx)
+    code = binding.MOE_EPI_F32 if epi == "f32" else binding.MOE_EPI_BF16
+    dt = torch.float32 if epi == "f32" else torch.bfloat16
+    out = torch.full((rows + 5, N), -7.0, dtype=dt, device="cuda")
+    binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, code, out, row_index=ri_d)
+    binding.check_device_status()
+    got = to_np(out).astype(np.float64)
+    Ag, sag = A[ridx], sa[ridx]
+    for g in range(G):
+        r0, r1 = offsets[g], offsets[g + 1]
+        if r1 == r0:
+            continue
+        exact = gemm_fp8(Ag[r0:r1], sag[r0:r1], B[g], sb[g])
+        mag = gemm_fp8(Ag[r0:r1] & 0x7F, sag[r0:r1], B[g] & 0x7F, sb[g])
+        err = np.abs(got[r0:r1] - exact)
+        if epi == "bf16":
+            assert np.all(err <= 2.0 ** -8 * np.abs(exact) + 1e-5 * mag + 1e-30), f"group {g}"
+            assert np.mean(got[r0:r1] == round_bf16(exact)) > 0.99
+        else:
+            assert np.all(err <= 1e-5 * mag + 1e-30), f"group {g}: {(err / mag).max():.3e}"
+    assert np.all(got[rows:] == -7.0)
+
+
+@gpu
+def test_gemm_gathered_swiglu_matches_plain():
+    """Gathered A rows through the SwiGLU epilogue give bit-identical h to the
+    same GEMM on the pre-gathered matrix (same tile order, same arithmetic)."""
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding
+    from oracle.quant import quant_128x128
+    rng = np.random.default_rng(11)
+    I, K, G, a_rows = 384, 512, 4, 500
+    sizes = [300, 0, 129, 1100]
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    rows = int(offsets[-1])
+    xq, xs = quant_1x128(rng.standard_normal((a_rows, K)).astype(np.float32))
+    W1 = [quant_128x128((rng.standard_normal((I, K)) / np.sqrt(K)).astype(np.float32)) for _ in range(G)]
+    W3 = [quant_128x128((rng.standard_normal((I, K)) / np.sqrt(K)).astype(np.float32)) for _ in range(G)]
+    q1 = np.stack([w[0] for w in W1]); s1 = np.stack([w[1] for w in W1])
+    q3 = np.stack([w[0] for w in W3]); s3 = np.stack([w[1] for w in W3])
+    ridx = _row_index(rng, rows, a_rows)
+    q1_d, s1_d, q3_d, s3_d, o_d, xq_d, xs_d, ri_d, xqg_d, xsg_d = _cuda(q1, s1, q3, s3, offsets, xq, xs, ridx,
+                                                                       xq[ridx], xs[ridx])
+    q13, s13 = binding.pack_w13(q1_d, s1_d, q3_d, s3_d)
+    outs = []
+    for gathered in (False, True):
+        hq = torch.full((rows, I), 0x55, dtype=torch.uint8, device="cuda")
+        hs = torch.full((rows, I // 128), -1.0, dtype=torch.float32, device="cuda")
+        if gathered:
+            binding.grouped_gemm_fp8(o_d, xq_d, xs_d, q13, s13, binding.MOE_EPI_SWIGLU_FP8, hq, hs, row_index=ri_d)
+        else:
+            binding.grouped_gemm_fp8(o_d, xqg_d, xsg_d, q13, s13, binding.MOE_EPI_SWIGLU_FP8, hq, hs)
+        binding.check_device_status()
+        outs.append((to_np(hq), to_np(hs)))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+@gpu
+def test_gemm_reports_out_of_range_row_index():
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding
+    offsets, A, sa, B, sb = _problem([10, 20, 30], 256, 128, seed=2)
+    ridx = np.arange(60, dtype=np.int32)
+    ridx[17] = A.shape[0]           # one past the last A row
+    o_d, A_d, sa_d, B_d, sb_d, ri_d = _cuda(offsets, A, sa, B, sb, ridx)
+    out = torch.zeros((60, 256), dtype=torch.bfloat16, device="cuda")
+    binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, binding.MOE_EPI_BF16, out, row_index=ri_d)
+    with pytest.raises(binding.MoeError) as e:
+        binding.check_device_status()
+    assert e.value.code == 6
+    binding.check_device_status()   # cleared
+
+
 @gpu
 def test_gemm_reports_corrupt_offsets():
     require_gpu()

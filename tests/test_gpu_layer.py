@@ -84,3 +84,25 @@ def test_layer_is_deterministic():
     y1 = layer.forward(x, update_bias=False).clone()
     y2 = layer.forward(x, update_bias=False).clone()
     assert torch.equal(y1, y2)
+
+
+@gpu
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_layer_token_row_modes_agree(name):
+    """Quantising straight into grouped rows, gathering a grouped copy, and
+    fetching token rows by index inside the gate/up GEMM give bit-identical
+    layer outputs."""
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding, inputs
+    from sparse_moe_layer_13_b300.layer import MoELayer
+    cfg = CONFIGS[name]
+    layers = {"scatter": MoELayer(cfg, "cuda")}
+    for mode in ("copy", "gather"):
+        layers[mode] = MoELayer(cfg, "cuda", weights=layers["scatter"].w, token_rows=mode)
+    x = inputs.gen_x(cfg, "cuda")
+    ys = {m: L.forward(x, update_bias=False).clone() for m, L in layers.items()}
+    binding.check_device_status()
+    for m in ("copy", "gather"):
+        assert torch.equal(ys["scatter"], ys[m]), m
+        assert torch.equal(layers["scatter"].hq, layers[m].hq) and torch.equal(layers["scatter"].hs, layers[m].hs)
+    assert torch.equal(layers["scatter"].xq_perm, layers["copy"].xq_perm)

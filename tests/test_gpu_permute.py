@@ -10,12 +10,12 @@ from oracle.quant import quant_1x128
 from sparse_moe_layer_13_b300.configs import CONFIGS, MoEConfig
 
 
-def _check(cfg, idx_np, seed=0):
+def _check(cfg, idx_np, seed=0, gather_rows=True):
     from sparse_moe_layer_13_b300 import binding, inputs
     x = inputs.gen_x(cfg, "cuda", step=seed)
     idx = torch.from_numpy(idx_np.astype(np.int32)).cuda()
     xq, xs = binding.quant_1x128(x)
-    out = binding.permute(cfg, idx, xq, xs, want_counts=True)
+    out = binding.permute(cfg, idx, xq, xs, want_counts=True, gather_rows=gather_rows)
     binding.check_device_status()
     offsets, sorted_token, row_of = oracle_permute(idx_np, cfg.E)
     T, K = cfg.T, cfg.K
@@ -23,10 +23,13 @@ def _check(cfg, idx_np, seed=0):
     assert np.array_equal(got_off[:cfg.E + 1], offsets)
     assert got_off[cfg.E + 1] == T * K + T
     assert np.array_equal(to_np(out["counts"]), histogram(idx_np, cfg.E))
-    assert np.array_equal(to_np(out["sorted_token"]), sorted_token)
+    src = np.concatenate([sorted_token, np.arange(T)])      # the shared expert's rows read token t
+    assert np.array_equal(to_np(out["sorted_token"]), src)
     assert np.array_equal(to_np(out["row_of"]), row_of)
+    if not gather_rows:
+        assert out["xq_perm"] is None
+        return
     rq, rs = quant_1x128(to_np(x))
-    src = np.concatenate([sorted_token, np.arange(T)])
     assert np.array_equal(to_np(out["xq_perm"]), rq[src])
     assert np.array_equal(to_np(out["xs_perm"]), rs[src])
 
@@ -42,6 +45,14 @@ def test_permute_workloads(name):
     require_gpu()
     cfg = CONFIGS[name]
     _check(cfg, _random_idx(cfg.T, cfg.E, cfg.K, 1))
+
+
+@gpu
+@pytest.mark.parametrize("name", ["tiny", "full"])
+def test_permute_without_row_gather(name):
+    require_gpu()
+    cfg = CONFIGS[name]
+    _check(cfg, _random_idx(cfg.T, cfg.E, cfg.K, 7), gather_rows=False)
 
 
 @gpu

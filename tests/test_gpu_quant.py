@@ -84,3 +84,53 @@ def test_pack_w13_layout():
         assert np.array_equal(Q13[:, base + 192:base + 256], Q3[:, 128 * j + 64:128 * j + 128])
         assert np.array_equal(to_np(s13)[:, 2 * j], to_np(s1)[:, j])
         assert np.array_equal(to_np(s13)[:, 2 * j + 1], to_np(s3)[:, j])
+
+
+def _scatter_case(T, d, E, K, seed):
+    from sparse_moe_layer_13_b300.configs import MoEConfig
+    cfg = MoEConfig("scatter", T=T, d=d, E=E, I=128, K=K, G=E // 16 if E >= 16 else 1, M=1, gk=1, seed=seed)
+    rng = np.random.default_rng(seed)
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    return cfg, idx
+
+
+@gpu
+@pytest.mark.parametrize("T,d,E,K", [(1, 128, 16, 1), (37, 256, 16, 4), (300, 7168, 256, 8), (1000, 1408, 64, 16)])
+def test_quant_1x128_scatter_bit_exact(T, d, E, K):
+    """Codes and scales land in grouped order: row row_of[t][k] and the
+    shared-expert row T*K + t each hold token t's quantised row."""
+    require_gpu()
+    from oracle.permute import permute as oracle_permute
+    from sparse_moe_layer_13_b300 import binding
+    cfg, idx = _scatter_case(T, d, E, K, T + d)
+    _, sorted_token, row_of = oracle_permute(idx, E)
+    x = _activation(T, d, T * 7 + d)
+    q, s = binding.quant_1x128_scatter(cfg, x, torch.from_numpy(row_of.astype(np.int32)).cuda())
+    binding.check_device_status()
+    rq, rs = quant_1x128(to_np(x))
+    src = np.concatenate([sorted_token, np.arange(T)])
+    assert np.array_equal(to_np(q), rq[src])
+    assert np.array_equal(to_np(s).view(np.uint32), rs[src].view(np.uint32))
+
+
+@gpu
+def test_quant_1x128_scatter_reports_bad_row():
+    require_gpu()
+    from oracle.permute import permute as oracle_permute
+    from sparse_moe_layer_13_b300 import binding
+    cfg, idx = _scatter_case(64, 256, 16, 4, 9)
+    _, sorted_token, row_of = oracle_permute(idx, 16)
+    row_of = row_of.astype(np.int32)
+    bad = row_of[5, 2]
+    row_of[5, 2] = cfg.T * cfg.K               # the first shared-expert row: not a routed row
+    x = _activation(cfg.T, cfg.d, 3)
+    q = torch.full((cfg.rows, cfg.d), 0x55, dtype=torch.uint8, device="cuda")
+    s = torch.full((cfg.rows, cfg.d // 128), -1.0, dtype=torch.float32, device="cuda")
+    binding.quant_1x128_scatter(cfg, x, torch.from_numpy(row_of).cuda(), q, s)
+    with pytest.raises(binding.MoeError) as e:
+        binding.check_device_status()
+    assert e.value.code == 6
+    binding.check_device_status()   # cleared
+    assert torch.all(q[bad] == 0x55)           # the slot the bad entry should have filled stays untouched
+    rq, _ = quant_1x128(to_np(x))
+    assert np.array_equal(to_np(q[cfg.T * cfg.K]), rq[0])   # shared row of token 0 written normally
