@@ -16,8 +16,9 @@
 //               thread: lane quadrant = warp % 4, column half = (warp-4)/4).
 //               After the last chunk: bf16 store, or SwiGLU + 1x128 E4M3
 //               requantisation of h.
-// The chunk accumulator is released as soon as it is read, so the tensor
-// cores run up to two chunks ahead of the promotion arithmetic.
+// The chunk accumulator is released as soon as its last TMEM load lands
+// (before the second half of the promotion FMAs), so the tensor cores run up
+// to two chunks ahead of the promotion arithmetic.
 //
 // Tiles: for each group, ceil(m_g / 128) row tiles x N/256 column tiles,
 // numbered group by group with the column tile fastest; CTA c takes tiles
@@ -47,6 +48,7 @@ constexpr uint32_t kRegsEpilogue = 232;
 constexpr int MAX_GROUPS = 1025;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = make_idesc(BM, BN, 0);
+
 
 struct Smem {
     uint64_t full[STAGES];
@@ -277,6 +279,13 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             prefetch(0);
             prefetch(1);
             prefetch(2);
+            // hands chunk buffer b back to the MMA issuer once this warp's loads from it have
+            // completed (before the last half of the promotion arithmetic, which runs on registers)
+            auto release = [&](uint32_t b) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.tempty[b]);
+            };
             float2 acc2[64];             // FP32 tile accumulator, column pairs
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
@@ -300,6 +309,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     tmem_ld_wait();
                     tmem_reg_fence(v0);
                     tmem_reg_fence(v1);
+                    if (r == 1) release(b);   // every value of the chunk is in registers now
                     const float2 ff = make_float2((r == 0) ? f0 : f1, (r == 0) ? f0 : f1);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -309,9 +319,6 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                                                            ff, acc2[r * 32 + 16 + i]);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.tempty[b]);
             }
             cp_async_wait<0>();
             float* acc = reinterpret_cast<float*>(acc2);

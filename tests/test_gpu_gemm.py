@@ -1,6 +1,6 @@
 """GPU parity: grouped FP8 GEMM (tcgen05) against the oracle's scaled FP8
-contraction, on ragged groups (empty, single-row, tile-straddling), both
-epilogues, and a corrupt offsets table."""
+contraction, on ragged groups (empty, single-row, tile-straddling), every
+epilogue, row-gathered A, and corrupt offsets or row indices."""
 import numpy as np
 import pytest
 import torch
@@ -37,6 +37,9 @@ SIZES = [
     [0, 1, 127, 128, 129, 300, 0, 513],
     [256],
     [5, 0, 0, 0, 1000],
+    # larger groups: several row tiles each, ragged last tiles, an empty
+    # group and groups of one tile plus one row
+    [700, 300, 1000, 0, 257, 129, 513],
 ]
 
 
