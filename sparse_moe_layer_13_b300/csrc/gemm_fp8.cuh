@@ -247,57 +247,87 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         const int rit = q * 32 + static_cast<int>(lane);
         const int et = ew * 32 + static_cast<int>(lane);
         const int nbn = p.N / 128;
+        // Chunk scales stream through a 4-slot shared-memory ring indexed by the chunk's
+        // position `it` in this CTA's sequence of chunks, copied (cp.async) three positions
+        // ahead. The look-ahead continues into the next tile, so a tile's first scales are in
+        // flight while the previous tile finishes; with fewer than three K chunks it would
+        // have to skip tiles, so each tile then starts its own copies.
+        struct ScaleRows { uint32_t sa; uint32_t sb; };   // element offsets of a tile's scale rows
+        auto scale_rows = [&](int tile) {
+            int g, mt, nt;
+            decode_tile(s, groups, ntiles, tile, g, mt, nt);
+            const int m_valid = s.row_start[g + 1] - s.row_start[g] - mt * BM;
+            int64_t src_row = rit < m_valid ? static_cast<int64_t>(s.row_start[g]) + mt * BM + rit : 0;
+            if (GATHER && rit < m_valid) {
+                src_row = __ldg(p.row_index + src_row);
+                if (src_row < 0 || src_row >= p.a_rows) src_row = 0;      // reported by the producer
+            }
+            // weight scale rows: SwiGLU -> gate block 2*nt (up block 2*nt+1 is nkc further on);
+            // otherwise block 2*nt+half. Offsets stay below 2^32 (checked at launch).
+            const int64_t sb0 = (static_cast<int64_t>(g) * nbn + 2 * nt + (EPI == MOE_EPI_SWIGLU_FP8 ? 0 : half)) * nkc;
+            return ScaleRows{static_cast<uint32_t>(src_row * nkc), static_cast<uint32_t>(sb0)};
+        };
+        // copies the scales of K chunk kc of the tile at `rows` into ring slot `slot`, as one group
+        auto copy_scales = [&](const ScaleRows& rows, int kc, uint32_t slot) {
+            cp_async_4(&s.ring_sa[slot][et], p.sa + rows.sa + kc);
+            if (lane == 0) {
+                cp_async_4(&s.ring_sb[slot][ew][0], p.sb + rows.sb + kc);
+                cp_async_4(&s.ring_sb[slot][ew][1], p.sb + rows.sb + (EPI == MOE_EPI_SWIGLU_FP8 ? nkc : 0) + kc);
+            }
+        };
+        // hands chunk buffer b back to the MMA issuer once this warp's loads from it have
+        // completed (before the last half of the promotion arithmetic, which runs on registers)
+        auto release = [&](uint32_t b) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.tempty[b]);
+        };
+        // (the all-FP32 store epilogue keeps per-tile copies: the look-ahead state makes it spill)
+        const bool ahead = EPI != MOE_EPI_F32 && nkc >= 3;
         uint32_t it = 0, tcount = 0;
         bool ok = true;
+        ScaleRows cur{0, 0}, nxt{0, 0};
+        if (ahead && static_cast<int>(blockIdx.x) < total) {
+            cur = scale_rows(blockIdx.x);
+            for (int j = 0; j < 3; ++j) {
+                copy_scales(cur, j, static_cast<uint32_t>(j));
+                cp_async_commit();
+            }
+        }
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
             int g, mt, nt;
             decode_tile(s, groups, ntiles, tile, g, mt, nt);
             const int m_valid = s.row_start[g + 1] - s.row_start[g] - mt * BM;
             const bool valid = rit < m_valid;
             const int64_t row = static_cast<int64_t>(s.row_start[g]) + mt * BM + rit;
-            int64_t src_row = valid ? row : 0;
-            if (GATHER && valid) {
-                src_row = __ldg(p.row_index + row);
-                if (src_row < 0 || src_row >= p.a_rows) src_row = 0;      // reported by the producer
-            }
-            const float* sa_row = p.sa + src_row * nkc;
-            // weight scale rows: SwiGLU -> gate block 2*nt, up block 2*nt+1; otherwise block 2*nt+half
-            const float* sb0 = p.sb + (static_cast<int64_t>(g) * nbn + 2 * nt + (EPI == MOE_EPI_SWIGLU_FP8 ? 0 : half)) * nkc;
-            const float* sb1 = (EPI == MOE_EPI_SWIGLU_FP8) ? sb0 + nkc : sb0;
-            // scales of chunk kc are fetched asynchronously three chunks ahead into a 4-slot ring
-            auto prefetch = [&](int kc) {
-                if (kc < nkc) {
-                    const int slot = kc & 3;
-                    cp_async_4(&s.ring_sa[slot][et], sa_row + kc);
-                    if (lane == 0) {
-                        cp_async_4(&s.ring_sb[slot][ew][0], sb0 + kc);
-                        cp_async_4(&s.ring_sb[slot][ew][1], sb1 + kc);
-                    }
+            const int next = tile + static_cast<int>(gridDim.x);
+            const bool has_next = next < total;
+            if (!ahead) {
+                cur = scale_rows(tile);
+                for (int j = 0; j < 3; ++j) {
+                    if (j < nkc) copy_scales(cur, j, (it + j) & 3u);
+                    cp_async_commit();
                 }
-                cp_async_commit();
-            };
-            prefetch(0);
-            prefetch(1);
-            prefetch(2);
-            // hands chunk buffer b back to the MMA issuer once this warp's loads from it have
-            // completed (before the last half of the promotion arithmetic, which runs on registers)
-            auto release = [&](uint32_t b) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s.tempty[b]);
-            };
+            }
+            if (ahead && has_next) nxt = scale_rows(next);
             float2 acc2[64];             // FP32 tile accumulator, column pairs
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
             for (int kc = 0; kc < nkc; ++kc, ++it) {
                 const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-                cp_async_wait<2>();
+                cp_async_wait<2>();      // this position's copies were the oldest of three groups
                 __syncwarp();
-                const int slot = kc & 3;
+                const uint32_t slot = it & 3u;
                 const float sav = s.ring_sa[slot][et];
                 const float f0 = sav * s.ring_sb[slot][ew][0];
                 const float f1 = sav * s.ring_sb[slot][ew][1];
-                prefetch(kc + 3);
+                // three positions ahead: this tile, else (look-ahead) the next one
+                const int k3 = kc + 3;
+                if (k3 < nkc)
+                    copy_scales(cur, k3, (it + 3) & 3u);
+                else if (ahead && has_next)
+                    copy_scales(nxt, k3 - nkc, (it + 3) & 3u);
+                cp_async_commit();
                 if (!mbar_wait(&s.tfull[b], bph, abort, kWaitLimitNs)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN + half * 128;
@@ -320,7 +350,6 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     }
                 }
             }
-            cp_async_wait<0>();
             float* acc = reinterpret_cast<float*>(acc2);
             if (!ok) break;
             const bool f32_out = (EPI == MOE_EPI_F32) || (EPI == MOE_EPI_BF16_F32_LAST && g == groups - 1);
@@ -388,7 +417,9 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     if (half == 0) p.out_aux[row * (I / 128) + nt] = sc;
                 }
             }
+            cur = nxt;
         }
+        cp_async_wait<0>();          // no scale copy may still target shared memory at exit
     }
 
     tc_fence_before();
