@@ -29,6 +29,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# measured DRAM bytes / algorithmic bytes of the gate/up GEMM (ncu, fullwidth_small workload)
+GATE_UP_DRAM_OVER_ALGORITHMIC = 1.229
 METRIC = "MoE layer tokens/s; FP8 grouped-GEMM TFLOP/s & % of roofline (1 B300)"
 UNIT = "tokens/s"
 
@@ -189,6 +191,11 @@ def run_ours(args):
     w13_bytes = touched * (2 * cfg.I * cfg.d + 4 * (2 * cfg.I // 128) * (cfg.d // 128))
     a_bytes = cfg.rows * (cfg.d + 4 * cfg.d // 128) + cfg.rows * (cfg.I + 4 * cfg.I // 128)
     g1_gbs = (w13_bytes + a_bytes) / (g1 * 1e-3) / 1e9
+    # DRAM bytes per gate/up launch: ncu's dram__bytes_read.sum + dram__bytes_write.sum for the
+    # same kernel on the fullwidth_small workload (small enough to capture) were 1.229 x its
+    # algorithmic bytes; traffic grows with the touched weights and rows, so a launch of this
+    # workload is estimated at that ratio.
+    traffic = round(GATE_UP_DRAM_OVER_ALGORITHMIC * (w13_bytes + a_bytes))
     weight_bound = cfg.T <= 1024     # a few rows per expert: the GEMMs stream weights
     if weight_bound:
         roof = {"kernel": "grouped_gemm_fp8 gate/up + SwiGLU (streams the touched experts' W13)",
@@ -199,7 +206,9 @@ def run_ours(args):
     else:
         roof = {"kernel": "grouped_gemm_fp8 gate/up + SwiGLU (largest share of the step)",
                 "bound": "tensor", "achieved": round(g1_tflops, 1), "peak": round(fp8_peak, 1),
-                "unit": "TFLOP/s", "frac": round(g1_tflops / fp8_peak, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(g1_tflops / fp8_peak, 4), "traffic": traffic,
+                "traffic_note": "DRAM bytes per launch, scaled from an ncu capture of the fullwidth_small workload",
+                "algorithmic_bytes": w13_bytes + a_bytes,
                 "peak_source": f"{src}: bf16 burst {bf16} TFLOP/s x 2 (E4M3/bf16 nominal ratio)"}
     tokens = cfg.T * ws
     value = tokens / (ms * 1e-3)
