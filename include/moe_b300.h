@@ -225,7 +225,9 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx,
  * h therefore matches an exact evaluation to a few FP32 ulps, not bit for
  * bit, and its E4M3 codes match except where that difference crosses a
  * rounding boundary.
- * N % 256 == 0, Kdim % 128 == 0. Rows outside every group are not written.
+ * N % 256 == 0, N <= 65536, Kdim % 128 == 0, rows * Kdim/128 and
+ * groups * N/128 * Kdim/128 below 2^32 (else MOE_ERR_UNSUPPORTED_SHAPE).
+ * Rows outside every group are not written.
  * Runs on the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA
  * operand loads); no workspace. */
 moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t rows,

@@ -46,6 +46,7 @@ constexpr int NUM_THREADS = 384;
 constexpr uint32_t kRegsProducer = 40;
 constexpr uint32_t kRegsEpilogue = 232;
 constexpr int MAX_GROUPS = 1025;
+constexpr int TILE_TAB = 1024;          // tiles per CTA decoded in the prologue (later ones: binary search)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = make_idesc(BM, BN, 0);
 
@@ -64,11 +65,13 @@ struct Smem {
     int row_start[MAX_GROUPS + 1];    // offsets[g]
     int mtile_prefix[MAX_GROUPS + 1]; // exclusive prefix of ceil(m_g / BM)
     float amax_x[2][8][32];
+    uint2 tile_tab[TILE_TAB];         // this CTA's tiles in order: {g | nt << 11 | min(m_valid,128) << 19, row0}
     float ring_sa[4][256];            // per-thread activation scale of chunks kc .. kc+3
     float ring_sb[4][8][2];           // per-warp weight scales (two 128-column blocks)
 };
 
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Smem);
+static_assert(SMEM_BYTES <= 227 * 1024, "more shared memory than a CTA may have");
 
 struct Params {
     const int32_t* offsets;
@@ -95,6 +98,32 @@ __device__ __forceinline__ void decode_tile(const Smem& s, int groups, int ntile
     }
     g = lo;
     mt = mtg - s.mtile_prefix[g];
+}
+
+// One tile's place: group, column tile, first grouped row, and valid rows
+// (m_valid, clipped to BM).
+struct TileInfo {
+    int g, nt, row0, m_valid;
+};
+
+__device__ __forceinline__ TileInfo tile_info_search(const Smem& s, int groups, int ntiles, int tile) {
+    int g, mt, nt;
+    decode_tile(s, groups, ntiles, tile, g, mt, nt);
+    const int row0 = s.row_start[g] + mt * BM;
+    return TileInfo{g, nt, row0, min(s.row_start[g + 1] - row0, BM)};
+}
+
+// k-th tile of this CTA (tile = blockIdx.x + k * gridDim.x): one shared-memory
+// load from the prologue's table (a binary search over the group prefix would
+// be nine dependent loads, slow while TMA and the tensor cores keep shared
+// memory busy)
+__device__ __forceinline__ TileInfo tile_info(const Smem& s, int groups, int ntiles, int k, int tile) {
+    if (k < TILE_TAB) {
+        const uint2 e = s.tile_tab[k];
+        return TileInfo{static_cast<int>(e.x & 2047u), static_cast<int>((e.x >> 11) & 255u), static_cast<int>(e.y),
+                        static_cast<int>(e.x >> 19)};
+    }
+    return tile_info_search(s, groups, ntiles, tile);
 }
 
 // GATHER: A rows are fetched by index (TMA gather4, four rows per copy)
@@ -158,11 +187,20 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             if (s.bad && blockIdx.x == 0) set_status(MOE_ERR_DEVICE_CHECK);
         }
     }
+    __syncthreads();
+    const int total = s.mtiles_total * ntiles;
+    for (int k = threadIdx.x; k < TILE_TAB; k += NUM_THREADS) {
+        const int tile = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+        if (tile >= total) break;
+        const TileInfo t = tile_info_search(s, groups, ntiles, tile);
+        s.tile_tab[k] = make_uint2(static_cast<uint32_t>(t.g) | (static_cast<uint32_t>(t.nt) << 11) |
+                                       (static_cast<uint32_t>(t.m_valid) << 19),
+                                   static_cast<uint32_t>(t.row0));
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem_base;
-    const int total = s.mtiles_total * ntiles;
     volatile int* abort = &s.abort;
 
     if (warp < 4) {
@@ -174,15 +212,14 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         // tile, indices held in registers for the whole tile).
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            int g, mt, nt;
-            decode_tile(s, groups, ntiles, tile, g, mt, nt);
-            const int row0 = s.row_start[g] + mt * BM;
-            const int brow = g * p.N + nt * BN;
+        for (int tile = blockIdx.x, k = 0; tile < total; tile += gridDim.x, ++k) {
+            const TileInfo t = tile_info(s, groups, ntiles, k, tile);
+            const int row0 = t.row0;
+            const int brow = t.g * p.N + t.nt * BN;
             int src[4] = {0, 0, 0, 0};
             if (GATHER) {
                 // rows past the group's end read row 0 (their results are dropped)
-                const int end = s.row_start[g + 1];
+                const int end = row0 + t.m_valid;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int r = row0 + 4 * static_cast<int>(lane) + q;
@@ -253,12 +290,10 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         // flight while the previous tile finishes; with fewer than three K chunks it would
         // have to skip tiles, so each tile then starts its own copies.
         struct ScaleRows { uint32_t sa; uint32_t sb; };   // element offsets of a tile's scale rows
-        auto scale_rows = [&](int tile) {
-            int g, mt, nt;
-            decode_tile(s, groups, ntiles, tile, g, mt, nt);
-            const int m_valid = s.row_start[g + 1] - s.row_start[g] - mt * BM;
-            int64_t src_row = rit < m_valid ? static_cast<int64_t>(s.row_start[g]) + mt * BM + rit : 0;
-            if (GATHER && rit < m_valid) {
+        auto scale_rows = [&](const TileInfo& t) {
+            const int g = t.g, nt = t.nt;
+            int64_t src_row = rit < t.m_valid ? static_cast<int64_t>(t.row0) + rit : 0;
+            if (GATHER && rit < t.m_valid) {
                 src_row = __ldg(p.row_index + src_row);
                 if (src_row < 0 || src_row >= p.a_rows) src_row = 0;      // reported by the producer
             }
@@ -288,28 +323,32 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         bool ok = true;
         ScaleRows cur{0, 0}, nxt{0, 0};
         if (ahead && static_cast<int>(blockIdx.x) < total) {
-            cur = scale_rows(blockIdx.x);
+            cur = scale_rows(tile_info(s, groups, ntiles, 0, blockIdx.x));
             for (int j = 0; j < 3; ++j) {
                 copy_scales(cur, j, static_cast<uint32_t>(j));
                 cp_async_commit();
             }
         }
+        // the first row of the last group (FP32 output rows of MOE_EPI_BF16_F32_LAST count from it)
+        const int last_start = s.row_start[groups - 1];
+        TileInfo tnext = static_cast<int>(blockIdx.x) < total ? tile_info(s, groups, ntiles, 0, blockIdx.x)
+                                                              : TileInfo{0, 0, 0, 0};
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
-            int g, mt, nt;
-            decode_tile(s, groups, ntiles, tile, g, mt, nt);
-            const int m_valid = s.row_start[g + 1] - s.row_start[g] - mt * BM;
-            const bool valid = rit < m_valid;
-            const int64_t row = static_cast<int64_t>(s.row_start[g]) + mt * BM + rit;
+            const TileInfo t = tnext;
+            const int g = t.g, nt = t.nt;
+            const bool valid = rit < t.m_valid;
+            const int64_t row = static_cast<int64_t>(t.row0) + rit;
             const int next = tile + static_cast<int>(gridDim.x);
             const bool has_next = next < total;
+            if (has_next) tnext = tile_info(s, groups, ntiles, static_cast<int>(tcount) + 1, next);
             if (!ahead) {
-                cur = scale_rows(tile);
+                cur = scale_rows(t);
                 for (int j = 0; j < 3; ++j) {
                     if (j < nkc) copy_scales(cur, j, (it + j) & 3u);
                     cp_async_commit();
                 }
             }
-            if (ahead && has_next) nxt = scale_rows(next);
+            if (ahead && has_next) nxt = scale_rows(tnext);
             float2 acc2[64];             // FP32 tile accumulator, column pairs
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
@@ -357,7 +396,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 if (valid) {
                     float* dst = (EPI == MOE_EPI_F32)
                                      ? static_cast<float*>(p.out) + row * p.N + nt * BN + half * 128
-                                     : p.out_aux + (row - s.row_start[g]) * p.N + nt * BN + half * 128;
+                                     : p.out_aux + (row - last_start) * p.N + nt * BN + half * 128;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         st_v8_b32(dst + 8 * i, __float_as_uint(acc[8 * i]), __float_as_uint(acc[8 * i + 1]),

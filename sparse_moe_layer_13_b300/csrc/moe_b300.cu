@@ -196,6 +196,7 @@ moe_status grouped_gemm(int32_t groups, const int32_t* offsets, int64_t rows, in
         a_rows >= INT32_MAX)
         return MOE_ERR_UNSUPPORTED_SHAPE;
     if (static_cast<int64_t>(groups) * N >= INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (N / gemm::BN > 256) return MOE_ERR_UNSUPPORTED_SHAPE;   // column tile index packed in 8 bits
     // the kernel addresses the scale arrays with 32-bit element offsets
     if ((row_index != nullptr ? a_rows : rows) * (Kdim / gemm::BK) >= UINT32_MAX ||
         static_cast<int64_t>(groups) * (N / 128) * (Kdim / gemm::BK) >= UINT32_MAX)
