@@ -134,6 +134,22 @@ class MoELayer:
             B.bias_update(c.E, c.T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
         return y
 
+    def capture(self, x: torch.Tensor, steps: int = 1, events=None, **forward_kw) -> torch.cuda.CUDAGraph:
+        """Records `steps` forwards of x into a CUDA graph; graph.replay() reruns them on
+        whatever x (a fixed device buffer) holds then, without per-launch host work.
+
+        forward_kw go to forward() (residual, update_bias, gamma, out); events, if given, is a
+        list of per-step event dicts as forward() takes, recorded inside the graph (create them
+        with torch.cuda.Event(enable_timing=True, external=True) to time replays). Every
+        library kernel must have run once before (one plain forward): a first launch sets
+        kernel attributes, which a capture does not record.
+        """
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(steps):
+                self.forward(x, events=None if events is None else events[i], **forward_kw)
+        return graph
+
     # library kernel launches per forward: route 5 (weight split, logits, selection, histogram,
     # scan), quantise 1, permute 3 (+1 row gather for "copy"), grouped GEMMs 2, combine 1,
     # bias update 1

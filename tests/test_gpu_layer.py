@@ -106,3 +106,30 @@ def test_layer_token_row_modes_agree(name):
         assert torch.equal(ys["scatter"], ys[m]), m
         assert torch.equal(layers["scatter"].hq, layers[m].hq) and torch.equal(layers["scatter"].hs, layers[m].hs)
     assert torch.equal(layers["scatter"].xq_perm, layers["copy"].xq_perm)
+
+
+@gpu
+def test_layer_graph_replay_matches_eager():
+    """A CUDA graph of two forwards (with the bias update) replays to the same
+    outputs and bias as the same two forwards run eagerly."""
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding, inputs
+    from sparse_moe_layer_13_b300.layer import MoELayer
+    cfg = CONFIGS["tiny"]
+    eager = MoELayer(cfg, "cuda")
+    graphed = MoELayer(cfg, "cuda", weights=eager.w)
+    x = inputs.gen_x(cfg, "cuda")
+    b0 = eager.bias.clone()
+    ys = []
+    for _ in range(2):
+        ys.append(eager.forward(x).clone())
+    graphed.forward(x, update_bias=False)         # first launches outside the capture
+    graphed.bias.copy_(b0)
+    g = graphed.capture(x, steps=2)
+    torch.cuda.synchronize()
+    assert torch.equal(graphed.bias, b0)          # capturing runs nothing
+    g.replay()
+    torch.cuda.synchronize()
+    binding.check_device_status()
+    assert torch.equal(graphed.y, ys[1])
+    assert torch.equal(graphed.bias, eager.bias)
