@@ -367,7 +367,8 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 else if (ahead && has_next)
                     copy_scales(nxt, k3 - nkc, (it + 3) & 3u);
                 cp_async_commit();
-                if (!mbar_wait(&s.tfull[b], bph, abort, kWaitLimitNs)) { ok = false; break; }
+                // warp-uniform outcome: every lane leaves together (warp syncs follow)
+                if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[b], bph, abort, kWaitLimitNs))) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN + half * 128;
 #pragma unroll
@@ -431,7 +432,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 // the partner warp (same quadrant, other half) holds the other 64 columns
                 s.amax_x[tcount & 1u][ew][lane] = amax;
                 mbar_arrive(&s.pair[q]);
-                if (!mbar_wait(&s.pair[q], tcount & 1u, abort, kWaitLimitNs)) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&s.pair[q], tcount & 1u, abort, kWaitLimitNs))) break;
                 amax = fmaxf(amax, s.amax_x[tcount & 1u][ew ^ 4][lane]);
                 const float sc = __fdiv_rn(amax, kE4M3Max);
                 // h is multiplied by the correctly rounded reciprocal of the scale
