@@ -54,20 +54,21 @@ def round_bf16(v) -> np.ndarray:
 
 
 class QuantExpert:
-    """One expert's weights quantised per 128x128 block."""
+    """One expert's weights quantised per 128x128 block (scale rule `rule`, see quant)."""
 
-    def __init__(self, w1, w3, w2):
-        self.q1, self.s1 = quant_128x128(w1)
-        self.q3, self.s3 = quant_128x128(w3)
-        self.q2, self.s2 = quant_128x128(w2)
+    def __init__(self, w1, w3, w2, rule: str = "fp32"):
+        self.rule = rule
+        self.q1, self.s1 = quant_128x128(w1, rule)
+        self.q3, self.s3 = quant_128x128(w3, rule)
+        self.q2, self.s2 = quant_128x128(w2, rule)
 
 
 def expert_forward(xq, xs, w: QuantExpert, return_h: bool = False):
-    """xq u8 [m][d], xs f32 [m][d/128] -> float64 [m][d]."""
+    """xq u8 [m][d], xs f32 [m][d/128] -> float64 [m][d]; h is quantised by the expert's rule."""
     gate = gemm_fp8(xq, xs, w.q1, w.s1)
     up = gemm_fp8(xq, xs, w.q3, w.s3)
     h = (silu(gate) * up).astype(np.float32)
-    hq, hs = quant_1x128(h)
+    hq, hs = quant_1x128(h, w.rule)
     out = gemm_fp8(hq, hs, w.q2, w.s2)
     if return_h:
         return out, h, hq, hs

@@ -53,8 +53,9 @@ class Layer:
     `experts` may pre-fill that cache with QuantExpert objects.
     """
 
-    def __init__(self, cfg, Wr, bias, expert_weights, logit_offset=None, experts=None):
+    def __init__(self, cfg, Wr, bias, expert_weights, logit_offset=None, experts=None, rule: str = "fp32"):
         self.cfg = cfg
+        self.rule = rule
         self.Wr = np.asarray(Wr, np.float32)
         self.bias = np.asarray(bias, np.float32)
         self.logit_offset = None if logit_offset is None else np.asarray(logit_offset, np.float32)
@@ -63,7 +64,7 @@ class Layer:
 
     def expert(self, e: int) -> QuantExpert:
         if e not in self._experts:
-            self._experts[e] = QuantExpert(*[np.asarray(w, np.float32) for w in self._weights(e)])
+            self._experts[e] = QuantExpert(*[np.asarray(w, np.float32) for w in self._weights(e)], rule=self.rule)
         return self._experts[e]
 
     def route(self, x):
@@ -81,7 +82,7 @@ class Layer:
         if idx is None:
             idx, gate, info = self.route(x)
         tokens = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
-        xq, xs = quant_1x128(x[tokens])
+        xq, xs = quant_1x128(x[tokens], self.rule)
         n = len(tokens)
         routed = np.zeros((n, c.K, c.d), dtype=np.float64)
         sub_idx = np.asarray(idx)[tokens]

@@ -10,13 +10,13 @@ from .ffn import QuantExpert
 
 
 def _one(job):
-    e, w1, w3, w2 = job
-    return e, QuantExpert(w1, w3, w2)
+    e, w1, w3, w2, rule = job
+    return e, QuantExpert(w1, w3, w2, rule)
 
 
-def quantize_experts(jobs, max_procs: int = 32) -> dict:
+def quantize_experts(jobs, max_procs: int = 32, rule: str = "fp32") -> dict:
     """jobs: iterable of (expert, W1, W3, W2) float32 arrays -> {expert: QuantExpert}."""
-    jobs = list(jobs)
+    jobs = [(*j, rule) for j in jobs]
     if len(jobs) <= 2:
         return dict(_one(j) for j in jobs)
     nproc = min(len(jobs), max(1, (os.cpu_count() or 2) - 1), max_procs)

@@ -22,7 +22,7 @@ def _make(cfg):
     return x, Wr, b, wts
 
 
-def _brute_token(cfg, x, Wr, b, layer, t):
+def _brute_token(cfg, x, Wr, b, layer, t, rule="fp32"):
     s = [1 / (1 + math.exp(-math.fsum(x[t, j] * Wr[e, j] for j in range(cfg.d)))) for e in range(cfg.E)]
     sb = [s[e] + float(b[e]) for e in range(cfg.E)]
     n = cfg.E // cfg.G
@@ -31,7 +31,7 @@ def _brute_token(cfg, x, Wr, b, layer, t):
     cand = [e for g in groups for e in range(g * n, (g + 1) * n)]
     chosen = max(itertools.combinations(cand, cfg.K), key=lambda c: sum(sb[e] for e in c))
     tot = sum(s[e] for e in chosen)
-    xq, xs = quant_1x128(x[t:t + 1])
+    xq, xs = quant_1x128(x[t:t + 1], rule)
     X = dequant_1x128(xq, xs)[0]
 
     def ffn(e):
@@ -39,7 +39,7 @@ def _brute_token(cfg, x, Wr, b, layer, t):
         W1, W3, W2 = (dequant_128x128(ex.q1, ex.s1), dequant_128x128(ex.q3, ex.s3), dequant_128x128(ex.q2, ex.s2))
         h = np.array([np.float32((lambda g, u: g / (1 + math.exp(-g)) * u)(
             math.fsum(X * W1[j]), math.fsum(X * W3[j]))) for j in range(cfg.I)], np.float32)
-        hq, hs = quant_1x128(h[None, :])
+        hq, hs = quant_1x128(h[None, :], rule)
         H = dequant_1x128(hq, hs)[0]
         return np.array([math.fsum(H * W2[i]) for i in range(cfg.d)])
 
@@ -58,6 +58,24 @@ def test_layer_matches_scalar_brute_force():
         assert set(res["idx"][t]) == chosen
         # the two sums of h may round to float32 differently in the last place
         assert np.max(np.abs(res["y"][t] - y)) <= 1e-6 * np.max(np.abs(y))
+
+
+def test_layer_pow2_rule_matches_scalar_brute_force():
+    """The power-of-two scale rule flows through every quantisation of the layer
+    (x, the weights and h): the layer equals the scalar evaluation with that rule."""
+    x, Wr, b, wts = _make(CFG)
+    layer = Layer(CFG, Wr, b, lambda e: wts[e], rule="pow2")
+    res = layer.forward(x)
+    for e in range(CFG.E + 1):
+        ex = layer.expert(e)
+        for sc in (ex.s1, ex.s3, ex.s2):
+            assert np.all(np.frexp(sc.astype(np.float64))[0] == 0.5)
+    for t in range(CFG.T):
+        chosen, y = _brute_token(CFG, x, Wr, b, layer, t, rule="pow2")
+        assert set(res["idx"][t]) == chosen
+        assert np.max(np.abs(res["y"][t] - y)) <= 1e-6 * np.max(np.abs(y))
+    ref = Layer(CFG, Wr, b, lambda e: wts[e]).forward(x)["y"]
+    assert not np.array_equal(res["y"], ref)      # a different quantisation rule gives different bytes
 
 
 def test_all_experts_special_case():

@@ -87,3 +87,65 @@ def test_dequant_close():
     q, s = quant_1x128(x)
     rel = np.linalg.norm(dequant_1x128(q, s) - x) / np.linalg.norm(x)
     assert rel < 0.04      # 3 mantissa bits: relative rounding error <= 2^-4 per element
+
+
+# ---- power-of-two (block-scaled MX) rule -----------------------------------
+
+def _pow2_by_search(amax: float) -> float:
+    """Smallest 2^e (e >= -126) with 448 * 2^e >= amax, by walking e upwards in exact arithmetic."""
+    if amax == 0:
+        return 0.0
+    a = Fraction(float(amax))
+    e = -160
+    while Fraction(448) * Fraction(2) ** e < a:
+        e += 1
+    return float(Fraction(2) ** max(e, -126))
+
+
+def test_pow2_scale_is_smallest_power_of_two_bound():
+    from oracle.quant import pow2_scale
+    rng = np.random.default_rng(4)
+    amax = np.concatenate([
+        (rng.standard_normal(300) ** 2 * 10.0 ** rng.integers(-30, 30, 300)).astype(np.float32),
+        np.float32([448.0, 447.99997, 448.00003, 1.75, 1.75 * 2 ** -20, 1.7500001, 3.5, 2.0 ** -120, 1e-40, 0.0]),
+    ])
+    got = pow2_scale(amax)
+    for a, s in zip(amax, got):
+        assert float(s) == _pow2_by_search(float(a)), (a, s)
+
+
+def test_pow2_quant_exact_shift_and_range():
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((24, 512)) * rng.uniform(1e-6, 1e6, (24, 1))).astype(np.float32)
+    q, s = quant_1x128(x, rule="pow2")
+    m, ex = np.frexp(s.astype(np.float64))
+    assert np.all(m == 0.5)                                   # powers of two
+    t = x.reshape(24, 4, 128).astype(np.float64)
+    r = t / s[:, :, None].astype(np.float64)
+    assert np.all(r * s[:, :, None] == t)                     # v / s is exact
+    amax = np.abs(t).max(axis=2)
+    assert np.all(amax / s <= 448) and np.all(amax / s > 224)  # smallest such power
+    # codes are the E4M3 rounding of the exact ratio
+    assert np.array_equal(q.reshape(24, 4, 128), e4m3.encode(r.astype(np.float32)))
+
+
+def test_pow2_clamp_and_zero_tiles():
+    x = np.zeros((3, 256), np.float32)
+    x[1, 5] = 2.0 ** -133                  # smallest bf16 subnormal: scale clamps to 2^-126
+    x[2, :128] = -0.0
+    q, s = quant_1x128(x, rule="pow2")
+    assert s[0, 0] == 0 and s[2, 0] == 0
+    assert s[1, 0] == np.float32(2.0 ** -126)
+    assert e4m3.decode(q[1:2, 5:6])[0, 0] * 2.0 ** -126 == 2.0 ** -133   # 2^-7 is an E4M3 subnormal
+    assert np.all(q[2, :128] == 0x80)
+
+
+def test_pow2_block_scales():
+    w = np.ones((256, 256), np.float32)
+    w[:128, 128:] *= 3.0
+    w[128:, :128] *= 1000.0
+    q, s = quant_128x128(w, rule="pow2")
+    assert s[0, 0] == np.float32(2.0 ** -8)      # 448 * 2^-8 = 1.75 >= 1 > 0.875
+    assert s[0, 1] == np.float32(2.0 ** -7)      # 3.5 >= 3
+    assert s[1, 0] == np.float32(2.0 ** 2)       # 1792 >= 1000 > 896
+    assert np.allclose(dequant_128x128(q, s), w, rtol=2 ** -4, atol=0)
