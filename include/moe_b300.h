@@ -139,6 +139,31 @@ moe_status moe_quant_fp8_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
 moe_status moe_quant_fp8_1x128_scatter(const moe_config* cfg, const uint16_t* x, const int32_t* row_of,
                                        uint8_t* xq_perm, float* xs_perm, void* stream);
 
+/* Scale rule of the FP8 quantisers below.
+ *   MOE_SCALE_FP32  scale = fl32(amax / 448), as above (the layer the pages
+ *                   describe; the default of the calls without a rule).
+ *   MOE_SCALE_POW2  scale = the smallest power of two s with 448 * s >= amax,
+ *                   at least 2^-126; 0 for an all-zero tile. Every scale is
+ *                   then an 8-bit exponent code, which the block-scaled
+ *                   GEMM (moe_grouped_gemm_fp8_mx) applies in the tensor
+ *                   core. The pages fix the tile shapes and the 448 bound
+ *                   ("DeepSeek-V3的MoE架构设计革新" §2 item 1, "DeepSeek-V3技术
+ *                   解析" §6.2) but not the scale's format; this is the
+ *                   second reading. v / s is exact and |v / s| <= 448. */
+typedef enum { MOE_SCALE_FP32 = 0, MOE_SCALE_POW2 = 1 } moe_scale_rule;
+
+/* moe_quant_fp8_1x128 with a scale rule (moe_scale_rule; else MOE_ERR_INVALID_ARG). */
+moe_status moe_quant_fp8_1x128_rule(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int32_t rule,
+                                    uint8_t* q, float* scale, void* stream);
+
+/* moe_quant_fp8_1x128_scatter with a scale rule. */
+moe_status moe_quant_fp8_1x128_scatter_rule(const moe_config* cfg, const uint16_t* x, const int32_t* row_of,
+                                            int32_t rule, uint8_t* xq_perm, float* xs_perm, void* stream);
+
+/* moe_quant_fp8_128x128 with a scale rule. */
+moe_status moe_quant_fp8_128x128_rule(const float* w, int64_t batch, int64_t rows, int64_t cols, int32_t rule,
+                                      uint8_t* q, float* scale, void* stream);
+
 /* Weight quantisation per 128x128 block, same rule as above with amax over
  * the block (same page, same item). Set-up only; `batch` independent
  * matrices stored back to back.

@@ -46,6 +46,9 @@ _SIG = {
     "moe_grouped_gemm_fp8_gather": (ctypes.c_int, [_I32, _P, _I64, _I32, _I32, _P, _P, _I64, _P, _P, _P, _I32, _P, _P,
                                                    _P]),
     "moe_quant_fp8_1x128_scatter": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
+    "moe_quant_fp8_1x128_rule": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P]),
+    "moe_quant_fp8_1x128_scatter_rule": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P]),
+    "moe_quant_fp8_128x128_rule": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_bias_update": (ctypes.c_int, [_I32, _I32, _I32, _P, ctypes.c_float, _P, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
@@ -84,6 +87,15 @@ def _call(name: str, *args) -> None:
     rc = getattr(load(), name)(*args)
     if rc != 0:
         raise MoeError(name, rc)
+
+
+SCALE_RULES = {"fp32": 0, "pow2": 1}     # moe_scale_rule
+
+
+def _rule(rule: str) -> int:
+    if rule not in SCALE_RULES:
+        raise ValueError(f"scale rule: {rule!r}")
+    return SCALE_RULES[rule]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -144,16 +156,16 @@ def route(cfg, x, Wr, bias, logit_offset=None, workspace=None, idx=None, gate=No
     return idx, gate, counts
 
 
-def quant_1x128(x, q=None, scale=None):
+def quant_1x128(x, q=None, scale=None, rule="fp32"):
     _need(x, torch.bfloat16, "x")
     rows, cols = x.shape
     q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device) if q is None else q
     scale = torch.empty(rows, cols // 128, dtype=torch.float32, device=x.device) if scale is None else scale
-    _call("moe_quant_fp8_1x128", _ptr(x), rows, cols, cols, _ptr(q), _ptr(scale), _stream())
+    _call("moe_quant_fp8_1x128_rule", _ptr(x), rows, cols, cols, _rule(rule), _ptr(q), _ptr(scale), _stream())
     return q, scale
 
 
-def quant_1x128_scatter(cfg, x, row_of, xq_perm=None, xs_perm=None):
+def quant_1x128_scatter(cfg, x, row_of, xq_perm=None, xs_perm=None, rule="fp32"):
     """Quantise tokens x [T][d] straight into grouped rows: row_of[t][k] and T*K + t."""
     _need(x, torch.bfloat16, "x", (cfg.T, cfg.d))
     _need(row_of, torch.int32, "row_of", (cfg.T, cfg.K))
@@ -163,12 +175,12 @@ def quant_1x128_scatter(cfg, x, row_of, xq_perm=None, xs_perm=None):
     _need(xq_perm, torch.uint8, "xq_perm", (rows, cfg.d))
     _need(xs_perm, torch.float32, "xs_perm", (rows, cfg.d // 128))
     c = config_c(cfg)
-    _call("moe_quant_fp8_1x128_scatter", ctypes.byref(c), _ptr(x), _ptr(row_of), _ptr(xq_perm), _ptr(xs_perm),
-          _stream())
+    _call("moe_quant_fp8_1x128_scatter_rule", ctypes.byref(c), _ptr(x), _ptr(row_of), _rule(rule), _ptr(xq_perm),
+          _ptr(xs_perm), _stream())
     return xq_perm, xs_perm
 
 
-def quant_128x128(w, q=None, scale=None):
+def quant_128x128(w, q=None, scale=None, rule="fp32"):
     """w float32 [rows][cols] or [batch][rows][cols]."""
     _need(w, torch.float32, "w")
     w3 = w if w.dim() == 3 else w.unsqueeze(0)
@@ -176,7 +188,7 @@ def quant_128x128(w, q=None, scale=None):
     q = torch.empty(w.shape, dtype=torch.uint8, device=w.device) if q is None else q
     sshape = (rows // 128, cols // 128) if w.dim() == 2 else (b, rows // 128, cols // 128)
     scale = torch.empty(sshape, dtype=torch.float32, device=w.device) if scale is None else scale
-    _call("moe_quant_fp8_128x128", _ptr(w), b, rows, cols, _ptr(q), _ptr(scale), _stream())
+    _call("moe_quant_fp8_128x128_rule", _ptr(w), b, rows, cols, _rule(rule), _ptr(q), _ptr(scale), _stream())
     return q, scale
 
 

@@ -39,6 +39,22 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
     return e4m3x2(a, b) | (e4m3x2(c, d) << 16);
 }
 
+// Scale of a tile with largest magnitude amax. FP32 rule: fl32(amax / 448).
+// Power-of-two rule (block-scaled variant): the smallest power of two s with
+// 448 * s >= amax, at least 2^-126; zero for amax == 0. With amax = m * 2^k,
+// m in [1, 2): 448 * 2^(k-8) = 1.75 * 2^k covers amax exactly when m <= 1.75,
+// i.e. when the mantissa field is at most 0x600000; otherwise 2^(k-7) does.
+template <bool POW2>
+__device__ __forceinline__ float tile_scale(float amax) {
+    if (!POW2) return __fdiv_rn(amax, kE4M3Max);
+    if (!(amax > 0.0f)) return 0.0f;
+    const uint32_t b = __float_as_uint(amax);
+    const int ef = static_cast<int>(b >> 23);                  // amax > 0: no sign bit
+    int e = ef - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    if (ef == 0 || e < -126) e = -126;                         // subnormal amax, or below the clamp
+    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
 // v / scale with IEEE rounding; an all-zero tile (scale 0) maps to signed zero.
 __device__ __forceinline__ float quant_ratio(float v, float scale) {
     return scale == 0.0f ? copysignf(0.0f, v) : __fdiv_rn(v, scale);

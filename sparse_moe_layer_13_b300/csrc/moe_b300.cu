@@ -336,41 +336,69 @@ moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr, 
     return MOE_OK;
 }
 
-moe_status moe_quant_fp8_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q, float* scale,
-                               void* stream) {
+moe_status moe_quant_fp8_1x128_rule(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int32_t rule,
+                                    uint8_t* q, float* scale, void* stream) {
     if (!x || !q || !scale || rows < 0 || cols < 0 || ld < cols) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scale) || ld % 8) return MOE_ERR_INVALID_ARG;
+    if (rule != MOE_SCALE_FP32 && rule != MOE_SCALE_POW2) return MOE_ERR_INVALID_ARG;
     if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0 || cols == 0) return MOE_OK;
     const int64_t tiles = rows * (cols / 128);
     // 8 warps per CTA, two tiles per warp step, two steps in flight per thread
     const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 32), static_cast<int64_t>(num_sms()) * 16));
-    quant_1x128_kernel<false><<<grid, 256, 0, as_stream(stream)>>>(x, rows, cols, ld, q, scale, nullptr, 0);
+    if (rule == MOE_SCALE_POW2)
+        quant_1x128_kernel<false, true><<<grid, 256, 0, as_stream(stream)>>>(x, rows, cols, ld, q, scale, nullptr, 0);
+    else
+        quant_1x128_kernel<false, false><<<grid, 256, 0, as_stream(stream)>>>(x, rows, cols, ld, q, scale, nullptr, 0);
+    return launch_status();
+}
+
+moe_status moe_quant_fp8_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, uint8_t* q, float* scale,
+                               void* stream) {
+    return moe_quant_fp8_1x128_rule(x, rows, cols, ld, MOE_SCALE_FP32, q, scale, stream);
+}
+
+moe_status moe_quant_fp8_1x128_scatter_rule(const moe_config* cfg, const uint16_t* x, const int32_t* row_of,
+                                            int32_t rule, uint8_t* xq_perm, float* xs_perm, void* stream) {
+    if (const moe_status st = check_config(cfg); st != MOE_OK) return st;
+    if (!x || !row_of || !xq_perm || !xs_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq_perm)) return MOE_ERR_INVALID_ARG;
+    if (rule != MOE_SCALE_FP32 && rule != MOE_SCALE_POW2) return MOE_ERR_INVALID_ARG;
+    const int64_t tiles = static_cast<int64_t>(cfg->T) * (cfg->d / 128);
+    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 32), static_cast<int64_t>(num_sms()) * 16));
+    if (rule == MOE_SCALE_POW2)
+        quant_1x128_kernel<true, true><<<grid, 256, 0, as_stream(stream)>>>(x, cfg->T, cfg->d, cfg->d, xq_perm,
+                                                                          xs_perm, row_of, cfg->K);
+    else
+        quant_1x128_kernel<true, false><<<grid, 256, 0, as_stream(stream)>>>(x, cfg->T, cfg->d, cfg->d, xq_perm,
+                                                                           xs_perm, row_of, cfg->K);
     return launch_status();
 }
 
 moe_status moe_quant_fp8_1x128_scatter(const moe_config* cfg, const uint16_t* x, const int32_t* row_of,
                                        uint8_t* xq_perm, float* xs_perm, void* stream) {
-    if (const moe_status st = check_config(cfg); st != MOE_OK) return st;
-    if (!x || !row_of || !xq_perm || !xs_perm) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(xq_perm)) return MOE_ERR_INVALID_ARG;
-    const int64_t tiles = static_cast<int64_t>(cfg->T) * (cfg->d / 128);
-    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 32), static_cast<int64_t>(num_sms()) * 16));
-    quant_1x128_kernel<true><<<grid, 256, 0, as_stream(stream)>>>(x, cfg->T, cfg->d, cfg->d, xq_perm, xs_perm,
-                                                                   row_of, cfg->K);
+    return moe_quant_fp8_1x128_scatter_rule(cfg, x, row_of, MOE_SCALE_FP32, xq_perm, xs_perm, stream);
+}
+
+moe_status moe_quant_fp8_128x128_rule(const float* w, int64_t batch, int64_t rows, int64_t cols, int32_t rule,
+                                      uint8_t* q, float* scale, void* stream) {
+    if (!w || !q || !scale || batch < 0 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(scale)) return MOE_ERR_INVALID_ARG;
+    if (rule != MOE_SCALE_FP32 && rule != MOE_SCALE_POW2) return MOE_ERR_INVALID_ARG;
+    if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int64_t blocks = batch * (rows / 128) * (cols / 128);
+    if (blocks == 0) return MOE_OK;
+    if (blocks > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rule == MOE_SCALE_POW2)
+        quant_128x128_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, as_stream(stream)>>>(w, rows, cols, q, scale);
+    else
+        quant_128x128_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, as_stream(stream)>>>(w, rows, cols, q, scale);
     return launch_status();
 }
 
 moe_status moe_quant_fp8_128x128(const float* w, int64_t batch, int64_t rows, int64_t cols, uint8_t* q, float* scale,
                                  void* stream) {
-    if (!w || !q || !scale || batch < 0 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(w) || !aligned16(q) || !aligned16(scale)) return MOE_ERR_INVALID_ARG;
-    if (rows % 128 || cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
-    const int64_t blocks = batch * (rows / 128) * (cols / 128);
-    if (blocks == 0) return MOE_OK;
-    if (blocks > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
-    quant_128x128_kernel<<<static_cast<unsigned>(blocks), 256, 0, as_stream(stream)>>>(w, rows, cols, q, scale);
-    return launch_status();
+    return moe_quant_fp8_128x128_rule(w, batch, rows, cols, MOE_SCALE_FP32, q, scale, stream);
 }
 
 moe_status moe_pack_w13(const uint8_t* q1, const float* s1, const uint8_t* q3, const float* s3, int64_t batch,

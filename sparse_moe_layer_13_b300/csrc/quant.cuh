@@ -1,7 +1,8 @@
 // Fine-grained FP8 quantisation ("DeepSeek-V3的MoE架构设计革新" §2 FP8 training,
 // item 1: activations per 1x128 tile, weights per 128x128 block; E4M3 largest
 // finite value 448 per "DeepSeek-V3技术解析" §6.2).
-//   scale = fl32(amax / 448), code = E4M3_RNE_SATFINITE(fl32(v / scale)).
+//   scale = fl32(amax / 448), code = E4M3_RNE_SATFINITE(fl32(v / scale));
+//   POW2 kernels take the power-of-two scale of tile_scale<true> instead.
 #pragma once
 
 #include "common.cuh"
@@ -17,7 +18,7 @@ namespace moe {
 // rows*K + r of q / scale instead of to row r (K <= 16: lane k of the half
 // warp loads row_of[r][k]). A grouped row outside [0, rows*K) is reported
 // and not written.
-template <bool SCATTER>
+template <bool SCATTER, bool POW2>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                           int64_t cols, int64_t ld, uint8_t* __restrict__ q,
                                                           float* __restrict__ scale,
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
                                fmaxf(fmaxf(fabsf(v4), fabsf(v5)), fmaxf(fabsf(v6), fabsf(v7))));
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float s = __fdiv_rn(amax, kE4M3Max);
+            const float s = tile_scale<POW2>(amax);
             uint2 codes;
             codes.x = e4m3x4(quant_ratio(v0, s), quant_ratio(v1, s), quant_ratio(v2, s), quant_ratio(v3, s));
             codes.y = e4m3x4(quant_ratio(v4, s), quant_ratio(v5, s), quant_ratio(v6, s), quant_ratio(v7, s));
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
 }
 
 // One CTA (256 threads) per 128x128 block of one matrix.
+template <bool POW2>
 __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restrict__ w, int64_t rows, int64_t cols,
                                                             uint8_t* __restrict__ q, float* __restrict__ scale) {
     const int64_t bc = cols / 128, br = rows / 128;
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float* __restr
     amax = red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-    const float s = __fdiv_rn(amax, kE4M3Max);
+    const float s = tile_scale<POW2>(amax);
     for (int i = 0; i < 16; ++i) {
         const float4 v = __ldg(reinterpret_cast<const float4*>(src + (tr + 8 * i) * cols + tc));
         *reinterpret_cast<uint32_t*>(dst + (tr + 8 * i) * cols + tc) =

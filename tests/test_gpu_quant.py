@@ -23,13 +23,14 @@ def _activation(rows, cols, seed):
 
 
 @gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
 @pytest.mark.parametrize("rows,cols", [(1, 128), (37, 256), (256, 7168), (4096, 2048), (129, 1408)])
-def test_quant_1x128_bit_exact(rows, cols):
+def test_quant_1x128_bit_exact(rows, cols, rule):
     require_gpu()
     from sparse_moe_layer_13_b300 import binding
     x = _activation(rows, cols, rows * 31 + cols)
-    q, s = binding.quant_1x128(x)
-    rq, rs = quant_1x128(to_np(x))
+    q, s = binding.quant_1x128(x, rule=rule)
+    rq, rs = quant_1x128(to_np(x), rule)
     assert np.array_equal(to_np(q), rq)
     assert np.array_equal(to_np(s).view(np.uint32), rs.view(np.uint32))
 
@@ -47,18 +48,19 @@ def test_quant_1x128_full_width_prefill_input():
 
 
 @gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
 @pytest.mark.parametrize("batch,rows,cols", [(1, 128, 128), (3, 256, 384), (2, 2048, 1408)])
-def test_quant_128x128_bit_exact(batch, rows, cols):
+def test_quant_128x128_bit_exact(batch, rows, cols, rule):
     require_gpu()
     from sparse_moe_layer_13_b300 import binding
     g = torch.Generator(device="cuda")
     g.manual_seed(batch * 7 + rows)
     w = torch.randn(batch, rows, cols, generator=g, device="cuda") / 40
     w[0, :128, :128] = 0
-    q, s = binding.quant_128x128(w)
+    q, s = binding.quant_128x128(w, rule=rule)
     wn = to_np(w)
     for b in range(batch):
-        rq, rs = quant_128x128(wn[b])
+        rq, rs = quant_128x128(wn[b], rule)
         assert np.array_equal(to_np(q[b]), rq)
         assert np.array_equal(to_np(s[b]), rs)
 
@@ -95,8 +97,9 @@ def _scatter_case(T, d, E, K, seed):
 
 
 @gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
 @pytest.mark.parametrize("T,d,E,K", [(1, 128, 16, 1), (37, 256, 16, 4), (300, 7168, 256, 8), (1000, 1408, 64, 16)])
-def test_quant_1x128_scatter_bit_exact(T, d, E, K):
+def test_quant_1x128_scatter_bit_exact(T, d, E, K, rule):
     """Codes and scales land in grouped order: row row_of[t][k] and the
     shared-expert row T*K + t each hold token t's quantised row."""
     require_gpu()
@@ -105,9 +108,9 @@ def test_quant_1x128_scatter_bit_exact(T, d, E, K):
     cfg, idx = _scatter_case(T, d, E, K, T + d)
     _, sorted_token, row_of = oracle_permute(idx, E)
     x = _activation(T, d, T * 7 + d)
-    q, s = binding.quant_1x128_scatter(cfg, x, torch.from_numpy(row_of.astype(np.int32)).cuda())
+    q, s = binding.quant_1x128_scatter(cfg, x, torch.from_numpy(row_of.astype(np.int32)).cuda(), rule=rule)
     binding.check_device_status()
-    rq, rs = quant_1x128(to_np(x))
+    rq, rs = quant_1x128(to_np(x), rule)
     src = np.concatenate([sorted_token, np.arange(T)])
     assert np.array_equal(to_np(q), rq[src])
     assert np.array_equal(to_np(s).view(np.uint32), rs[src].view(np.uint32))
