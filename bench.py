@@ -126,7 +126,7 @@ def run_ours(args):
         dist.barrier()
     cfg = {**CONFIGS, **PROFILE_CONFIGS}[args.config]
     offset = inputs.gen_logit_offset(cfg, cfg.zipf_c, dev) if cfg.zipf_s else None
-    layer = MoELayer(cfg, dev, logit_offset=offset)
+    layer = MoELayer(cfg, dev, logit_offset=offset, scale_rule=args.scales)
     skew = None
     if cfg.skew_steps:
         skew = balancing_loop(cfg, layer, dev, binding, inputs, dp)
@@ -231,7 +231,9 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic (seeded N(0,1) x, N(0,1/d) weights, random init)",
-        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E}+1 I={cfg.I} K={cfg.K} G={cfg.G} M={cfg.M}",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E}+1 I={cfg.I} K={cfg.K} G={cfg.G} M={cfg.M}"
+                               + (" (power-of-two scales, block-scaled GEMMs)" if args.scales == "pow2" else ""),
+                   "scale_rule": args.scales,
                    "tokens_per_gpu": cfg.T, "global_tokens": tokens, "parallelism": f"dp{ws}",
                    "launch": "one CUDA graph of the K steps" if graph is not None else "eager launches",
                    "l2": (f"inputs exceed L2: x {cfg.T * cfg.d * 2 / 1e6:.0f} MB and FP8 expert weights "
@@ -398,6 +400,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph of the K steps")
+    ap.add_argument("--scales", default="fp32", choices=["fp32", "pow2"],
+                    help="pow2: power-of-two 1x128 / 128x128 scales and the block-scaled GEMMs")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -261,6 +261,19 @@ moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t 
                                 const uint8_t* B, const float* sb,
                                 int32_t epilogue, void* out, float* out_aux, void* stream);
 
+/* moe_grouped_gemm_fp8 for power-of-two scales (MOE_SCALE_POW2): the same
+ * result, computed by the block-scaled tensor-core MMA
+ * (tcgen05.mma.kind::mxf8f6f4.block_scale) that applies each K=32 step's
+ * scales 2^ea * 2^eb from 8-bit exponent codes, so the whole K reduction of
+ * a tile accumulates in one TMEM accumulator. sa and sb must hold powers of
+ * two or zero (as moe_quant_*_rule(MOE_SCALE_POW2) writes them); any other
+ * value sets MOE_ERR_DEVICE_CHECK. The SwiGLU epilogue quantises h with the
+ * power-of-two rule. Arguments, layouts and other errors as
+ * moe_grouped_gemm_fp8. */
+moe_status moe_grouped_gemm_fp8_mx(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,
+                                   const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
+                                   int32_t epilogue, void* out, float* out_aux, void* stream);
+
 /* moe_grouped_gemm_fp8 with the A operand gathered by row: grouped row r
  * reads row row_index[r] of A [a_rows][Kdim] and of sa [a_rows][Kdim/128]
  * (TMA gather, four rows per copy), e.g. the unpermuted quantised tokens with

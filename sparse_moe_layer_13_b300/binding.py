@@ -49,6 +49,7 @@ _SIG = {
     "moe_quant_fp8_1x128_rule": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P]),
     "moe_quant_fp8_1x128_scatter_rule": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P]),
     "moe_quant_fp8_128x128_rule": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P]),
+    "moe_grouped_gemm_fp8_mx": (ctypes.c_int, [_I32, _P, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_bias_update": (ctypes.c_int, [_I32, _I32, _I32, _P, ctypes.c_float, _P, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
@@ -258,11 +259,12 @@ def permute_noalloc(cfg, idx, xq, xs, out=None, want_counts=False):
 
 
 def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out_scale=None, last_rows=None,
-                     row_index=None):
+                     row_index=None, block_scaled=False):
     """offsets i32 [G+1]; A u8 [rows][K]; sa f32 [rows][K/128]; B u8 [G][N][K]; sb f32 [G][N/128][K/128].
 
     out_scale is the auxiliary output: h scales for the SwiGLU epilogue, or
     the FP32 output of the last group (last_rows rows) for MOE_EPI_BF16_F32_LAST.
+    block_scaled: power-of-two scales, run on the block-scaled MMA (moe_grouped_gemm_fp8_mx).
     """
     groups = offsets.numel() - 1
     a_rows, Kdim = A.shape
@@ -287,7 +289,12 @@ def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out
         out = torch.empty(rows, N // 2, dtype=torch.uint8, device=A.device) if out is None else out
         out_scale = (torch.empty(rows, N // 256, dtype=torch.float32, device=A.device)
                      if out_scale is None else out_scale)
-    if row_index is None:
+    if block_scaled:
+        if row_index is not None:
+            raise ValueError("the block-scaled GEMM reads A in grouped row order (no row_index)")
+        _call("moe_grouped_gemm_fp8_mx", groups, _ptr(offsets), rows, N, Kdim, _ptr(A), _ptr(sa), _ptr(B), _ptr(sb),
+              epilogue, _ptr(out), _ptr(out_scale), _stream())
+    elif row_index is None:
         _call("moe_grouped_gemm_fp8", groups, _ptr(offsets), rows, N, Kdim, _ptr(A), _ptr(sa), _ptr(B), _ptr(sb),
               epilogue, _ptr(out), _ptr(out_scale), _stream())
     else:

@@ -88,7 +88,8 @@ struct Params {
 };
 
 // tile -> (group, row tile inside the group, column tile)
-__device__ __forceinline__ void decode_tile(const Smem& s, int groups, int ntiles, int tile, int& g, int& mt, int& nt) {
+template <typename SmemT>
+__device__ __forceinline__ void decode_tile(const SmemT& s, int groups, int ntiles, int tile, int& g, int& mt, int& nt) {
     const int mtg = tile / ntiles;
     nt = tile - mtg * ntiles;
     int lo = 0, hi = groups - 1;           // last g with mtile_prefix[g] <= mtg
@@ -106,7 +107,8 @@ struct TileInfo {
     int g, nt, row0, m_valid;
 };
 
-__device__ __forceinline__ TileInfo tile_info_search(const Smem& s, int groups, int ntiles, int tile) {
+template <typename SmemT>
+__device__ __forceinline__ TileInfo tile_info_search(const SmemT& s, int groups, int ntiles, int tile) {
     int g, mt, nt;
     decode_tile(s, groups, ntiles, tile, g, mt, nt);
     const int row0 = s.row_start[g] + mt * BM;
@@ -117,13 +119,94 @@ __device__ __forceinline__ TileInfo tile_info_search(const Smem& s, int groups, 
 // load from the prologue's table (a binary search over the group prefix would
 // be nine dependent loads, slow while TMA and the tensor cores keep shared
 // memory busy)
-__device__ __forceinline__ TileInfo tile_info(const Smem& s, int groups, int ntiles, int k, int tile) {
+template <typename SmemT>
+__device__ __forceinline__ TileInfo tile_info(const SmemT& s, int groups, int ntiles, int k, int tile) {
     if (k < TILE_TAB) {
         const uint2 e = s.tile_tab[k];
         return TileInfo{static_cast<int>(e.x & 2047u), static_cast<int>((e.x >> 11) & 255u), static_cast<int>(e.y),
                         static_cast<int>(e.x >> 19)};
     }
     return tile_info_search(s, groups, ntiles, tile);
+}
+
+// The finished FP32 tile accumulator of this thread (row `rit` of the tile, 128 columns
+// of column half `half`) to the output: FP32 rows, bf16 rows, or SwiGLU + 1x128 E4M3
+// requantisation of h (scale rule POW2 or FP32). Returns false if the amax exchange with
+// the partner warp timed out.
+template <int EPI, bool POW2, typename SmemT>
+__device__ __forceinline__ bool store_tile(float* acc, const Params& p, SmemT& s, const TileInfo& t, int groups,
+                                           int last_start, int rit, int half, int ew, int q, uint32_t lane,
+                                           uint32_t tcount, volatile int* abort) {
+    const int g = t.g, nt = t.nt;
+    const bool valid = rit < t.m_valid;
+    const int64_t row = static_cast<int64_t>(t.row0) + rit;
+        const bool f32_out = (EPI == MOE_EPI_F32) || (EPI == MOE_EPI_BF16_F32_LAST && g == groups - 1);
+        if (f32_out) {
+            if (valid) {
+                float* dst = (EPI == MOE_EPI_F32)
+                                 ? static_cast<float*>(p.out) + row * p.N + nt * BN + half * 128
+                                 : p.out_aux + (row - last_start) * p.N + nt * BN + half * 128;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    st_v8_b32(dst + 8 * i, __float_as_uint(acc[8 * i]), __float_as_uint(acc[8 * i + 1]),
+                              __float_as_uint(acc[8 * i + 2]), __float_as_uint(acc[8 * i + 3]),
+                              __float_as_uint(acc[8 * i + 4]), __float_as_uint(acc[8 * i + 5]),
+                              __float_as_uint(acc[8 * i + 6]), __float_as_uint(acc[8 * i + 7]));
+            }
+        } else if (EPI == MOE_EPI_BF16 || EPI == MOE_EPI_BF16_F32_LAST) {
+            if (valid) {
+                uint16_t* dst = static_cast<uint16_t*>(p.out) + row * p.N + nt * BN + half * 128;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    st_v8_b32(dst + 16 * i, pack_bf16x2(acc[16 * i + 0], acc[16 * i + 1]),
+                              pack_bf16x2(acc[16 * i + 2], acc[16 * i + 3]),
+                              pack_bf16x2(acc[16 * i + 4], acc[16 * i + 5]),
+                              pack_bf16x2(acc[16 * i + 6], acc[16 * i + 7]),
+                              pack_bf16x2(acc[16 * i + 8], acc[16 * i + 9]),
+                              pack_bf16x2(acc[16 * i + 10], acc[16 * i + 11]),
+                              pack_bf16x2(acc[16 * i + 12], acc[16 * i + 13]),
+                              pack_bf16x2(acc[16 * i + 14], acc[16 * i + 15]));
+            }
+        } else {
+            // h = SiLU(gate) * up for this thread's 64 columns; gate in acc[0,64), up in acc[64,128)
+            float amax = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float gte = acc[c];
+                const float h = __fdividef(gte * acc[64 + c], 1.0f + __expf(-gte));
+                acc[c] = h;
+                amax = fmaxf(amax, fabsf(h));
+            }
+            // the partner warp (same quadrant, other half) holds the other 64 columns
+            s.amax_x[tcount & 1u][ew][lane] = amax;
+            mbar_arrive(&s.pair[q]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.pair[q], tcount & 1u, abort, kWaitLimitNs))) return false;
+            amax = fmaxf(amax, s.amax_x[tcount & 1u][ew ^ 4][lane]);
+            const float sc = tile_scale<POW2>(amax);
+            // h is multiplied by the correctly rounded reciprocal of the scale (exact for
+            // a power of two; otherwise one rounding more than the quotient, enough for an
+            // E4M3 code)
+            const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+            if (valid) {
+                const int I = p.N / 2;
+                uint8_t* dst = static_cast<uint8_t*>(p.out) + row * I + nt * 128 + half * 64;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint4 w;
+                    w.x = e4m3x4(rs * acc[16 * i + 0], rs * acc[16 * i + 1],
+                                 rs * acc[16 * i + 2], rs * acc[16 * i + 3]);
+                    w.y = e4m3x4(rs * acc[16 * i + 4], rs * acc[16 * i + 5],
+                                 rs * acc[16 * i + 6], rs * acc[16 * i + 7]);
+                    w.z = e4m3x4(rs * acc[16 * i + 8], rs * acc[16 * i + 9],
+                                 rs * acc[16 * i + 10], rs * acc[16 * i + 11]);
+                    w.w = e4m3x4(rs * acc[16 * i + 12], rs * acc[16 * i + 13],
+                                 rs * acc[16 * i + 14], rs * acc[16 * i + 15]);
+                    reinterpret_cast<uint4*>(dst)[i] = w;
+                }
+                if (half == 0) p.out_aux[row * (I / 128) + nt] = sc;
+            }
+        }
+    return true;
 }
 
 // GATHER: A rows are fetched by index (TMA gather4, four rows per copy)
@@ -392,71 +475,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             }
             float* acc = reinterpret_cast<float*>(acc2);
             if (!ok) break;
-            const bool f32_out = (EPI == MOE_EPI_F32) || (EPI == MOE_EPI_BF16_F32_LAST && g == groups - 1);
-            if (f32_out) {
-                if (valid) {
-                    float* dst = (EPI == MOE_EPI_F32)
-                                     ? static_cast<float*>(p.out) + row * p.N + nt * BN + half * 128
-                                     : p.out_aux + (row - last_start) * p.N + nt * BN + half * 128;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        st_v8_b32(dst + 8 * i, __float_as_uint(acc[8 * i]), __float_as_uint(acc[8 * i + 1]),
-                                  __float_as_uint(acc[8 * i + 2]), __float_as_uint(acc[8 * i + 3]),
-                                  __float_as_uint(acc[8 * i + 4]), __float_as_uint(acc[8 * i + 5]),
-                                  __float_as_uint(acc[8 * i + 6]), __float_as_uint(acc[8 * i + 7]));
-                }
-            } else if (EPI == MOE_EPI_BF16 || EPI == MOE_EPI_BF16_F32_LAST) {
-                if (valid) {
-                    uint16_t* dst = static_cast<uint16_t*>(p.out) + row * p.N + nt * BN + half * 128;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        st_v8_b32(dst + 16 * i, pack_bf16x2(acc[16 * i + 0], acc[16 * i + 1]),
-                                  pack_bf16x2(acc[16 * i + 2], acc[16 * i + 3]),
-                                  pack_bf16x2(acc[16 * i + 4], acc[16 * i + 5]),
-                                  pack_bf16x2(acc[16 * i + 6], acc[16 * i + 7]),
-                                  pack_bf16x2(acc[16 * i + 8], acc[16 * i + 9]),
-                                  pack_bf16x2(acc[16 * i + 10], acc[16 * i + 11]),
-                                  pack_bf16x2(acc[16 * i + 12], acc[16 * i + 13]),
-                                  pack_bf16x2(acc[16 * i + 14], acc[16 * i + 15]));
-                }
-            } else {
-                // h = SiLU(gate) * up for this thread's 64 columns; gate in acc[0,64), up in acc[64,128)
-                float amax = 0.0f;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const float gte = acc[c];
-                    const float h = __fdividef(gte * acc[64 + c], 1.0f + __expf(-gte));
-                    acc[c] = h;
-                    amax = fmaxf(amax, fabsf(h));
-                }
-                // the partner warp (same quadrant, other half) holds the other 64 columns
-                s.amax_x[tcount & 1u][ew][lane] = amax;
-                mbar_arrive(&s.pair[q]);
-                if (!__all_sync(0xffffffffu, mbar_wait(&s.pair[q], tcount & 1u, abort, kWaitLimitNs))) break;
-                amax = fmaxf(amax, s.amax_x[tcount & 1u][ew ^ 4][lane]);
-                const float sc = __fdiv_rn(amax, kE4M3Max);
-                // h is multiplied by the correctly rounded reciprocal of the scale
-                // (one rounding more than the quotient, enough for an E4M3 code)
-                const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
-                if (valid) {
-                    const int I = p.N / 2;
-                    uint8_t* dst = static_cast<uint8_t*>(p.out) + row * I + nt * 128 + half * 64;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 w;
-                        w.x = e4m3x4(rs * acc[16 * i + 0], rs * acc[16 * i + 1],
-                                     rs * acc[16 * i + 2], rs * acc[16 * i + 3]);
-                        w.y = e4m3x4(rs * acc[16 * i + 4], rs * acc[16 * i + 5],
-                                     rs * acc[16 * i + 6], rs * acc[16 * i + 7]);
-                        w.z = e4m3x4(rs * acc[16 * i + 8], rs * acc[16 * i + 9],
-                                     rs * acc[16 * i + 10], rs * acc[16 * i + 11]);
-                        w.w = e4m3x4(rs * acc[16 * i + 12], rs * acc[16 * i + 13],
-                                     rs * acc[16 * i + 14], rs * acc[16 * i + 15]);
-                        reinterpret_cast<uint4*>(dst)[i] = w;
-                    }
-                    if (half == 0) p.out_aux[row * (I / 128) + nt] = sc;
-                }
-            }
+            if (!store_tile<EPI, false>(acc, p, s, t, groups, last_start, rit, half, ew, q, lane, tcount, abort)) break;
             cur = nxt;
         }
         cp_async_wait<0>();          // no scale copy may still target shared memory at exit

@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "gemm_fp8.cuh"
+#include "gemm_mx.cuh"
 #include "misc.cuh"
 #include "permute.cuh"
 #include "quant.cuh"
@@ -179,11 +180,26 @@ moe_status launch_gemm_epi(int32_t epilogue, const CUtensorMap& ta, const CUtens
     return launch_gemm<MOE_EPI_SWIGLU_FP8, GATHER>(ta, tb, p, tiles_max, st);
 }
 
+template <int EPI>
+moe_status launch_gemm_mx(const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p, int64_t tiles_max,
+                          cudaStream_t st) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemm_mx::grouped_gemm_mx_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(gemm_mx::SMEM_BYTES)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set = true;
+    }
+    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_max, 1)));
+    gemm_mx::grouped_gemm_mx_kernel<EPI><<<grid, gemm::NUM_THREADS, gemm_mx::SMEM_BYTES, st>>>(ta, tb, p);
+    return launch_status();
+}
+
 // Shared checks and launch of the grouped GEMM; row_index == nullptr: A is in grouped row order.
 moe_status grouped_gemm(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,
                         const uint8_t* A, const float* sa, int64_t a_rows, const int32_t* row_index,
                         const uint8_t* B, const float* sb, int32_t epilogue, void* out, float* out_aux,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool block_scaled = false) {
     if (!offsets || !A || !sa || !B || !sb || !out || rows < 0 || a_rows < 0 || groups < 1 || N < 0 || Kdim < 0)
         return MOE_ERR_INVALID_ARG;
     if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8 && epilogue != MOE_EPI_F32 &&
@@ -212,6 +228,12 @@ moe_status grouped_gemm(int32_t groups, const int32_t* offsets, int64_t rows, in
         return MOE_ERR_CUDA;
     gemm::Params p{offsets, groups, rows, N, Kdim, sa, sb, out, out_aux, row_index, a_rows};
     const int64_t tiles_max = (ceil_div(rows, gemm::BM) + groups) * (N / gemm::BN);
+    if (block_scaled) {
+        if (epilogue == MOE_EPI_BF16) return launch_gemm_mx<MOE_EPI_BF16>(ta, tb, p, tiles_max, st);
+        if (epilogue == MOE_EPI_F32) return launch_gemm_mx<MOE_EPI_F32>(ta, tb, p, tiles_max, st);
+        if (epilogue == MOE_EPI_BF16_F32_LAST) return launch_gemm_mx<MOE_EPI_BF16_F32_LAST>(ta, tb, p, tiles_max, st);
+        return launch_gemm_mx<MOE_EPI_SWIGLU_FP8>(ta, tb, p, tiles_max, st);
+    }
     if (gather) return launch_gemm_epi<true>(epilogue, ta, tb, p, tiles_max, st);
     return launch_gemm_epi<false>(epilogue, ta, tb, p, tiles_max, st);
 }
@@ -490,6 +512,13 @@ moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t 
                                 void* out, float* out_aux, void* stream) {
     return grouped_gemm(groups, offsets, rows, N, Kdim, A, sa, rows, nullptr, B, sb, epilogue, out, out_aux,
                         as_stream(stream));
+}
+
+moe_status moe_grouped_gemm_fp8_mx(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,
+                                   const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
+                                   int32_t epilogue, void* out, float* out_aux, void* stream) {
+    return grouped_gemm(groups, offsets, rows, N, Kdim, A, sa, rows, nullptr, B, sb, epilogue, out, out_aux,
+                        as_stream(stream), true);
 }
 
 moe_status moe_grouped_gemm_fp8_gather(int32_t groups, const int32_t* offsets, int64_t rows, int32_t N, int32_t Kdim,

@@ -15,6 +15,9 @@ token_rows picks how the gate/up GEMM gets its grouped token rows:
              (moe_grouped_gemm_fp8_gather: no grouped copy, (K+1)*T*d fewer
              bytes of device memory, slower GEMM).
 All three give bit-identical results.
+
+scale_rule "pow2" quantises x, the weights and h with power-of-two scales and
+runs both grouped GEMMs on the block-scaled MMA (moe_grouped_gemm_fp8_mx).
 """
 from __future__ import annotations
 
@@ -26,14 +29,16 @@ from .configs import MoEConfig
 
 
 class ExpertWeights:
-    """FP8 expert weights on the device, built from the seeded generator.
+    """FP8 expert weights on the device, built from the seeded generator, with
+    128x128 scales under `scale_rule` ("fp32" or "pow2").
 
     q13 u8 [E+1][2I][d] (SwiGLU layout), s13 f32 [E+1][2I/128][d/128],
     q2  u8 [E+1][d][I],                  s2  f32 [E+1][d/128][I/128].
     """
 
-    def __init__(self, cfg: MoEConfig, device="cuda", chunk: int = 16):
+    def __init__(self, cfg: MoEConfig, device="cuda", chunk: int = 16, scale_rule: str = "fp32"):
         E1, I, d = cfg.E + 1, cfg.I, cfg.d
+        self.scale_rule = scale_rule
         self.q13 = torch.empty(E1, 2 * I, d, dtype=torch.uint8, device=device)
         self.s13 = torch.empty(E1, 2 * I // 128, d // 128, dtype=torch.float32, device=device)
         self.q2 = torch.empty(E1, d, I, dtype=torch.uint8, device=device)
@@ -45,10 +50,10 @@ class ExpertWeights:
             w3 = torch.stack([w[1] for w in ws])
             w2 = torch.stack([w[2] for w in ws])
             del ws
-            q1, s1 = B.quant_128x128(w1)
-            q3, s3 = B.quant_128x128(w3)
+            q1, s1 = B.quant_128x128(w1, rule=scale_rule)
+            q3, s3 = B.quant_128x128(w3, rule=scale_rule)
             B.pack_w13(q1, s1, q3, s3, self.q13[e0:e1], self.s13[e0:e1])
-            B.quant_128x128(w2, self.q2[e0:e1], self.s2[e0:e1])
+            B.quant_128x128(w2, self.q2[e0:e1], self.s2[e0:e1], rule=scale_rule)
             del w1, w3, w2, q1, q3
 
 
@@ -56,16 +61,24 @@ class MoELayer:
     """One layer instance: router weight, selection bias, expert weights, buffers."""
 
     def __init__(self, cfg: MoEConfig, device="cuda", weights: ExpertWeights | None = None,
-                 logit_offset: torch.Tensor | None = None, token_rows: str = "scatter"):
+                 logit_offset: torch.Tensor | None = None, token_rows: str = "scatter", scale_rule: str = "fp32"):
         if token_rows not in ("scatter", "copy", "gather"):
             raise ValueError(f"token_rows: {token_rows!r}")
+        if scale_rule not in ("fp32", "pow2"):
+            raise ValueError(f"scale_rule: {scale_rule!r}")
+        if scale_rule == "pow2" and token_rows == "gather":
+            raise ValueError("the block-scaled GEMM reads grouped rows; use token_rows 'scatter' or 'copy'")
         self.cfg = cfg
         self.token_rows = token_rows
+        self.scale_rule = scale_rule
+        self.block_scaled = scale_rule == "pow2"
         self.device = device
         self.Wr = inputs.gen_router(cfg, device)
         self.bias = inputs.gen_bias(cfg, device)
         self.logit_offset = logit_offset
-        self.w = ExpertWeights(cfg, device) if weights is None else weights
+        self.w = ExpertWeights(cfg, device, scale_rule=scale_rule) if weights is None else weights
+        if self.w.scale_rule != scale_rule:
+            raise ValueError("the expert weights were quantised with another scale rule")
         T, K, E, d, I = cfg.T, cfg.K, cfg.E, cfg.d, cfg.I
         R = cfg.rows
         z = lambda *s, dt: torch.empty(*s, dtype=dt, device=device)  # noqa: E731
@@ -104,11 +117,12 @@ class MoELayer:
         ev = events or {}
         B.route(c, x, self.Wr, self.bias, self.logit_offset, self.ws, self.idx, self.gate, self.counts)
         mode = self.token_rows
+        rule = self.scale_rule
         if mode != "scatter":
-            B.quant_1x128(x, self.xq, self.xs)
+            B.quant_1x128(x, self.xq, self.xs, rule=rule)
         B.permute(c, self.idx, self.xq, self.xs, self.ws, self.perm, gather_rows=mode == "copy")
         if mode == "scatter":
-            B.quant_1x128_scatter(c, x, self.perm["row_of"], self.xq_perm, self.xs_perm)
+            B.quant_1x128_scatter(c, x, self.perm["row_of"], self.xq_perm, self.xs_perm, rule=rule)
         if "gemm1" in ev:
             ev["gemm1"][0].record()
         if mode == "gather":
@@ -116,13 +130,13 @@ class MoELayer:
                                self.hq, self.hs, row_index=self.perm["sorted_token"])
         else:
             B.grouped_gemm_fp8(self.perm["offsets"], self.xq_perm, self.xs_perm, self.w.q13, self.w.s13,
-                               B.MOE_EPI_SWIGLU_FP8, self.hq, self.hs)
+                               B.MOE_EPI_SWIGLU_FP8, self.hq, self.hs, block_scaled=self.block_scaled)
         if "gemm1" in ev:
             ev["gemm1"][1].record()
         if "gemm2" in ev:
             ev["gemm2"][0].record()
         B.grouped_gemm_fp8(self.perm["offsets"], self.hq, self.hs, self.w.q2, self.w.s2, B.MOE_EPI_BF16_F32_LAST,
-                           self.out, self.out_shared)
+                           self.out, self.out_shared, block_scaled=self.block_scaled)
         if "gemm2" in ev:
             ev["gemm2"][1].record()
         TK = c.T * c.K

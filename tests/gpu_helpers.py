@@ -49,7 +49,7 @@ def assert_y_close(got, want):
     return rel, mx
 
 
-def oracle_experts(cfg, experts, device="cuda"):
+def oracle_experts(cfg, experts, device="cuda", rule="fp32"):
     """Quantised oracle experts for `experts`, built in parallel CPU workers.
 
     The fp32 weights come from the same seeded generator (on `device`) that
@@ -58,7 +58,7 @@ def oracle_experts(cfg, experts, device="cuda"):
     from oracle.parallel import quantize_experts
     from sparse_moe_layer_13_b300.inputs import gen_expert
     jobs = [(e, *(to_np(w) for w in gen_expert(cfg, e, device))) for e in sorted(set(int(e) for e in experts))]
-    return quantize_experts(jobs)
+    return quantize_experts(jobs, rule=rule)
 
 
 def check_routing(cfg, idx_gpu, gate_gpu, ref_idx, ref_gate, info):

@@ -13,10 +13,10 @@ from oracle.route import near_tie, route as oracle_route
 from sparse_moe_layer_13_b300.configs import CONFIGS
 
 
-def _layer_case(cfg, n_sample=None, residual=False, seed=0):
+def _layer_case(cfg, n_sample=None, residual=False, seed=0, rule="fp32"):
     from sparse_moe_layer_13_b300 import binding, inputs
     from sparse_moe_layer_13_b300.layer import MoELayer
-    layer = MoELayer(cfg, "cuda")
+    layer = MoELayer(cfg, "cuda", scale_rule=rule)
     x = inputs.gen_x(cfg, "cuda")
     b0 = to_np(layer.bias).copy()
     y = to_np(layer.forward(x, residual=residual, update_bias=True))
@@ -31,9 +31,9 @@ def _layer_case(cfg, n_sample=None, residual=False, seed=0):
         rng = np.random.default_rng(seed)
         tokens = np.sort(rng.choice(np.nonzero(~tie)[0], n_sample, replace=False))
     needed = set(ref_idx[tokens].ravel().tolist()) | {cfg.E}
-    ex = oracle_experts(cfg, needed)
-    ref = Layer(cfg, Wr, b0, None, experts=ex).forward(xn, tokens=tokens, idx=ref_idx, gate=ref_gate,
-                                                       residual=residual)
+    ex = oracle_experts(cfg, needed, rule=rule)
+    ref = Layer(cfg, Wr, b0, None, experts=ex, rule=rule).forward(xn, tokens=tokens, idx=ref_idx, gate=ref_gate,
+                                                                  residual=residual)
     keep = ~tie[tokens]
     rel, mx = assert_y_close(y[tokens][keep], ref["y"][keep])
     # end-of-step bias update, bit-exact, from the oracle's own load
@@ -133,3 +133,18 @@ def test_layer_graph_replay_matches_eager():
     binding.check_device_status()
     assert torch.equal(graphed.y, ys[1])
     assert torch.equal(graphed.bias, eager.bias)
+
+
+@gpu
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_layer_pow2_block_scaled(name):
+    """Power-of-two scales throughout, both GEMMs on the block-scaled MMA,
+    against the oracle's layer with the same scale rule."""
+    require_gpu()
+    _layer_case(CONFIGS[name], rule="pow2")
+
+
+@gpu
+def test_layer_pow2_block_scaled_full_width_sampled():
+    require_gpu()
+    _layer_case(CONFIGS["full"], n_sample=48, seed=5, rule="pow2")
