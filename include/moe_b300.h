@@ -186,6 +186,26 @@ moe_status moe_pack_w13(const uint8_t* q1, const float* s1, const uint8_t* q3, c
                         int64_t batch, int64_t I, int64_t d,
                         uint8_t* q13, float* s13, void* stream);
 
+/* Sequence-wise balance statistics and loss ("《DeepSeek-V3 Technical Report》
+ * 深度解读报告" §2.3: beside the auxiliary-loss-free bias, a balance loss L_Bal
+ * of very small weight alpha keeps a single sequence from extreme imbalance;
+ * the page gives no formula, this is the plainest reading). Tokens form
+ * sequences of seq_len consecutive tokens; for sequence q:
+ *   f[q][i] = E / (K * seq_len) * (number of its tokens that chose expert i)
+ *   P[q][i] = mean over its tokens t of s[t][i] / sum_j s[t][j]
+ *   loss[q] = alpha * sum_i f[q][i] * P[q][i]
+ * with s the unbiased affinities (sigmoid of the logits plus logit_offset).
+ * Call after moe_route on the same workspace and stream: the router logits it
+ * left there are read back, so logit_offset must be the one moe_route got.
+ *   topk_idx  device i32 [T][K], moe_route's output
+ *   seq_len   multiple of 32 dividing T (else MOE_ERR_UNSUPPORTED_SHAPE)
+ *   f, P      device f32 [T/seq_len][E] out, or NULL
+ *   loss      device f32 [T/seq_len] out
+ * Deterministic (fixed summation order, no atomics). */
+moe_status moe_balance_loss(const moe_config* cfg, const float* logit_offset, const int32_t* topk_idx,
+                            int32_t seq_len, float alpha, float* f, float* P, float* loss, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* Token permutation by expert (expert histogram, exclusive prefix sum and a
  * stable scatter, all without atomics), then a gather of the quantised
  * rows into grouped order. Rows are ordered by (expert, token); the shared

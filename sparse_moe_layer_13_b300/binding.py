@@ -50,6 +50,7 @@ _SIG = {
     "moe_quant_fp8_1x128_scatter_rule": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P]),
     "moe_quant_fp8_128x128_rule": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P]),
     "moe_grouped_gemm_fp8_mx": (ctypes.c_int, [_I32, _P, _I64, _I32, _I32, _P, _P, _P, _P, _I32, _P, _P, _P]),
+    "moe_balance_loss": (ctypes.c_int, [_P, _P, _P, _I32, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_bias_update": (ctypes.c_int, [_I32, _I32, _I32, _P, ctypes.c_float, _P, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
@@ -301,6 +302,21 @@ def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out
         _call("moe_grouped_gemm_fp8_gather", groups, _ptr(offsets), rows, N, Kdim, _ptr(A), _ptr(sa), a_rows,
               _ptr(row_index), _ptr(B), _ptr(sb), epilogue, _ptr(out), _ptr(out_scale), _stream())
     return out, out_scale
+
+
+def balance_loss(cfg, idx, workspace, seq_len, alpha, logit_offset=None, stats=True):
+    """Per-sequence L_Bal after moe_route on `workspace`; returns (loss [T/seq_len], f, P) with
+    f, P [T/seq_len][E] (None unless stats)."""
+    _need(idx, torch.int32, "topk_idx", (cfg.T, cfg.K))
+    nseq = cfg.T // seq_len
+    dev = idx.device
+    loss = torch.empty(nseq, dtype=torch.float32, device=dev)
+    f = torch.empty(nseq, cfg.E, dtype=torch.float32, device=dev) if stats else None
+    P = torch.empty(nseq, cfg.E, dtype=torch.float32, device=dev) if stats else None
+    c = config_c(cfg)
+    _call("moe_balance_loss", ctypes.byref(c), _ptr(logit_offset), _ptr(idx), seq_len, alpha, _ptr(f), _ptr(P),
+          _ptr(loss), _ptr(workspace), workspace.numel(), _stream())
+    return loss, f, P
 
 
 def combine(cfg, routed_out, shared_out, row_of, gate, residual=None, y=None):

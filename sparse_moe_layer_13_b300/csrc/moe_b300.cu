@@ -69,9 +69,9 @@ int route_ksplit(const moe_config* c) {
 
 // Workspace layout: [router logit partials f32 ksplit*T*E][router weight
 // planes bf16 3*E*d][per-block counts i32 nblk*E][per-block bases i32
-// nblk*E][offsets scratch i32 E+2]
+// nblk*E][offsets scratch i32 E+2][balance chunk sums f32, i32 (T/32)*E each]
 struct WsLayout {
-    size_t logits, planes, blk_counts, blk_base, offsets, total;
+    size_t logits, planes, blk_counts, blk_base, offsets, balance, total;
 };
 
 WsLayout ws_layout(const moe_config* c) {
@@ -82,7 +82,9 @@ WsLayout ws_layout(const moe_config* c) {
     w.blk_counts = w.planes + align_up(static_cast<size_t>(3) * c->E * c->d * sizeof(uint16_t), 256);
     w.blk_base = w.blk_counts + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
     w.offsets = w.blk_base + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
-    w.total = w.offsets + align_up(static_cast<size_t>(c->E + 2) * sizeof(int32_t), 256);
+    w.balance = w.offsets + align_up(static_cast<size_t>(c->E + 2) * sizeof(int32_t), 256);
+    // balance statistics: per-32-token-chunk sums, f32 [T/32][E] then i32 [T/32][E]
+    w.total = w.balance + 2 * align_up(static_cast<size_t>(ceil_div(c->T, 32)) * c->E * sizeof(float), 256);
     return w;
 }
 
@@ -278,6 +280,14 @@ moe_status permute_scratch(int32_t** out) {
     return MOE_OK;
 }
 
+template <int EPL>
+void launch_balance_partial(const float* z, int ks, const moe_config* c, const float* offset, const int32_t* idx,
+                            float* p_part, int32_t* c_part, cudaStream_t st) {
+    const int nchunk = c->T / 32;
+    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(nchunk, 4), static_cast<int64_t>(num_sms()) * 8));
+    route::balance_partial_kernel<EPL><<<grid, 128, 0, st>>>(z, ks, c->T, c->E, c->K, offset, idx, p_part, c_part);
+}
+
 }  // namespace
 
 extern "C" {
@@ -467,6 +477,34 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, const uin
     const int64_t rows = npairs + cfg->T;
     perm::gather_kernel<<<static_cast<unsigned>(ceil_div(rows * 32, 256)), 256, 0, st>>>(
         sorted_token, cfg->T, cfg->K, cfg->d, xq, xs, xq_perm, xs_perm);
+    return launch_status();
+}
+
+moe_status moe_balance_loss(const moe_config* cfg, const float* logit_offset, const int32_t* topk_idx,
+                            int32_t seq_len, float alpha, float* f, float* P, float* loss, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    if (const moe_status st = check_config(cfg); st != MOE_OK) return st;
+    if (!topk_idx || !loss || !workspace) return MOE_ERR_INVALID_ARG;
+    if (seq_len < 32 || seq_len % 32 || cfg->T % seq_len) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const WsLayout w = ws_layout(cfg);
+    if (workspace_bytes < w.total) return MOE_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const float* z = reinterpret_cast<const float*>(ws + w.logits);
+    float* p_part = reinterpret_cast<float*>(ws + w.balance);
+    int32_t* c_part = reinterpret_cast<int32_t*>(
+        ws + w.balance + align_up(static_cast<size_t>(ceil_div(cfg->T, 32)) * cfg->E * sizeof(float), 256));
+    const int ks = route_ksplit(cfg);
+    const cudaStream_t st = as_stream(stream);
+    const int epl = (cfg->E + 31) / 32;
+    if (epl <= 8)
+        launch_balance_partial<8>(z, ks, cfg, logit_offset, topk_idx, p_part, c_part, st);
+    else if (epl <= 16)
+        launch_balance_partial<16>(z, ks, cfg, logit_offset, topk_idx, p_part, c_part, st);
+    else
+        launch_balance_partial<32>(z, ks, cfg, logit_offset, topk_idx, p_part, c_part, st);
+    const int nseq = cfg->T / seq_len;
+    route::balance_final_kernel<<<ceil_div(nseq, 4), 128, 0, st>>>(p_part, c_part, nseq, seq_len, cfg->E, cfg->K,
+                                                                   alpha, f, P, loss);
     return launch_status();
 }
 

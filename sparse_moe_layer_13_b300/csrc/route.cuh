@@ -115,3 +115,98 @@ select_kernel(const float* __restrict__ z, int ksplit, int T, int E, int G, int 
 
 }  // namespace route
 }  // namespace moe
+
+namespace moe {
+namespace route {
+
+// Sequence-wise balance statistics (《DeepSeek-V3 Technical Report》深度解读报告 §2.3:
+// L_Bal with a very small weight; read as L = alpha * sum_i f_i * P_i per sequence,
+// f_i = E / (K L) * #{t : i chosen by t}, P_i = mean over t of s[t][i] / sum_j s[t][j]).
+//
+// balance_partial_kernel: one warp per 32-token chunk (chunks never straddle a
+// sequence); lane l holds experts l, l+32, ... The affinities are recomputed from
+// the router's K-split logits exactly as the selection computes them; the token's
+// sum over experts is a fixed butterfly. Per-chunk sums of s / sum and of choice
+// counts go to p_part / c_part [chunk][E].
+template <int EPL>
+__global__ void __launch_bounds__(128)
+balance_partial_kernel(const float* __restrict__ z, int ksplit, int T, int E, int K, const float* __restrict__ offset,
+                       const int32_t* __restrict__ topk_idx, float* __restrict__ p_part, int32_t* __restrict__ c_part) {
+    const int lane = static_cast<int>(lane_id());
+    const int nchunk = T / 32;
+    const int64_t TE = static_cast<int64_t>(T) * E;
+    for (int c = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < nchunk; c += (gridDim.x * blockDim.x) >> 5) {
+        float p[EPL];
+        int cnt[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) { p[i] = 0.0f; cnt[i] = 0; }
+        for (int t = c * 32; t < c * 32 + 32; ++t) {
+            const float* zt = z + static_cast<int64_t>(t) * E;
+            float s[EPL];
+            float local = 0.0f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int e = lane + 32 * i;
+                s[i] = 0.0f;
+                if (e < E) {
+                    float zz = __ldg(zt + e);
+                    for (int sp_i = 1; sp_i < ksplit; ++sp_i) zz += __ldg(zt + sp_i * TE + e);
+                    if (offset != nullptr) zz += __ldg(offset + e);
+                    s[i] = __fdiv_rn(1.0f, 1.0f + expf(-zz));
+                    local += s[i];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+            const int mine = lane < K ? __ldg(topk_idx + static_cast<int64_t>(t) * K + lane) : -1;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) p[i] += __fdiv_rn(s[i], local);
+            for (int k = 0; k < K; ++k) {
+                const int ek = __shfl_sync(0xffffffffu, mine, k);
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) cnt[i] += (ek == lane + 32 * i) ? 1 : 0;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                p_part[static_cast<int64_t>(c) * E + e] = p[i];
+                c_part[static_cast<int64_t>(c) * E + e] = cnt[i];
+            }
+        }
+    }
+}
+
+// One warp per sequence: chunk sums in chunk order, then f, P and the loss
+// (the sum over experts in a fixed order: lanes, then a butterfly).
+__global__ void __launch_bounds__(128)
+balance_final_kernel(const float* __restrict__ p_part, const int32_t* __restrict__ c_part, int nseq, int seq_len,
+                     int E, int K, float alpha, float* __restrict__ f_out, float* __restrict__ p_out,
+                     float* __restrict__ loss_out) {
+    const int lane = static_cast<int>(lane_id());
+    const int q = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (q >= nseq) return;
+    const int cps = seq_len / 32;                      // chunks per sequence
+    const float fscale = static_cast<float>(E) / (static_cast<float>(K) * static_cast<float>(seq_len));
+    float acc = 0.0f;
+    for (int e = lane; e < E; e += 32) {
+        float ps = 0.0f;
+        int cs = 0;
+        for (int c = q * cps; c < (q + 1) * cps; ++c) {
+            ps += p_part[static_cast<int64_t>(c) * E + e];
+            cs += c_part[static_cast<int64_t>(c) * E + e];
+        }
+        const float P = ps / static_cast<float>(seq_len);
+        const float f = fscale * static_cast<float>(cs);
+        if (f_out != nullptr) f_out[static_cast<int64_t>(q) * E + e] = f;
+        if (p_out != nullptr) p_out[static_cast<int64_t>(q) * E + e] = P;
+        acc += f * P;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) loss_out[q] = alpha * acc;
+}
+
+}  // namespace route
+}  // namespace moe

@@ -148,6 +148,12 @@ class MoELayer:
             B.bias_update(c.E, c.T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
         return y
 
+    def balance_loss(self, seq_len: int, alpha: float, stats: bool = False):
+        """Sequence-wise balance loss of the last forward's routing (loss per sequence of
+        seq_len tokens, and f, P [sequences][E] if stats); reads the router logits that the
+        forward left in the workspace, so call it before the next forward."""
+        return B.balance_loss(self.cfg, self.idx, self.ws, seq_len, alpha, self.logit_offset, stats)
+
     def capture(self, x: torch.Tensor, steps: int = 1, events=None, **forward_kw) -> torch.cuda.CUDAGraph:
         """Records `steps` forwards of x into a CUDA graph; graph.replay() reruns them on
         whatever x (a fixed device buffer) holds then, without per-launch host work.

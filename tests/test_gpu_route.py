@@ -60,3 +60,27 @@ def test_route_all_groups_all_experts():
     _run(cfg)
     cfg = MoEConfig("g1", T=100, d=128, E=32, I=128, K=5, G=1, M=1, gk=3, seed=10, bias="uniform")
     _run(cfg)
+
+
+@gpu
+@pytest.mark.parametrize("name,seq_len", [("tiny", 64), ("mid", 1024), ("full", 4096)])
+def test_balance_loss_matches_oracle(name, seq_len):
+    """Sequence-wise balance statistics from the router's own logits against
+    the oracle's FP64 affinities and the GPU's routing."""
+    require_gpu()
+    from oracle.balance import balance_stats
+    from oracle.route import affinity
+    from sparse_moe_layer_13_b300 import binding, inputs
+    cfg = CONFIGS[name]
+    x = inputs.gen_x(cfg, "cuda")
+    Wr = inputs.gen_router(cfg, "cuda")
+    bias = inputs.gen_bias(cfg, "cuda")
+    ws = torch.empty(binding.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    idx, gate, _ = binding.route(cfg, x, Wr, bias, None, ws)
+    loss, f, P = binding.balance_loss(cfg, idx, ws, seq_len, 1e-4)
+    binding.check_device_status()
+    s = affinity(to_np(x), to_np(Wr))
+    rf, rP = balance_stats(s, to_np(idx), seq_len)
+    assert np.allclose(to_np(f), rf, rtol=1e-6, atol=0)          # counts exact; E / (K L) rounded in FP32
+    assert np.allclose(to_np(P), rP, rtol=1e-5, atol=1e-9)
+    assert np.allclose(to_np(loss), 1e-4 * (rf * rP).sum(axis=1), rtol=1e-5, atol=0)
