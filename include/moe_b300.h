@@ -77,7 +77,13 @@ typedef enum moe_epilogue {
     /* out: bf16 [rows][N] for every group but the last; out_aux: f32
      * [offsets[groups] - offsets[groups-1]][N] for the last group (the
      * shared expert, whose output enters the layer output with gate 1). */
-    MOE_EPI_BF16_F32_LAST = 3
+    MOE_EPI_BF16_F32_LAST = 3,
+    /* The SwiGLU pre-activations, unreduced: B laid out as for
+     * MOE_EPI_SWIGLU_FP8; out: f32 [rows][N] in that tile layout (for I-block
+     * j, columns 256j.. hold gate[128j..+64), up[128j..+64), gate[128j+64..
+     * +128), up[128j+64..+128)). The backward pass recomputes them with this
+     * epilogue; the values equal those the SwiGLU epilogue reduces. */
+    MOE_EPI_GATEUP_F32 = 4
 } moe_epilogue;
 
 /* Human-readable name of a status. Never NULL. */
@@ -328,6 +334,136 @@ moe_status moe_combine(const moe_config* cfg, const uint16_t* routed_out, const 
  *   counts device i32 [E]; bias device f32 [E] in/out. */
 moe_status moe_bias_update(int32_t E, int32_t T, int32_t K, const int32_t* counts,
                            float gamma, float* bias, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Backward pass of the layer.
+ *
+ * The pages frame the FP8 recipe as training ("DeepSeek-V3的MoE架构设计革新"
+ * §2 FP8 training) and the bias as acting on expert choice only
+ * (《DeepSeek-V3 Technical Report》深度解读报告 §2.3); they print no backward
+ * pass. These calls compute the plain one with the chosen experts held
+ * fixed: gradients flow through the gates g = s/sum(s), the sigmoid
+ * affinities s and the SwiGLU experts, not through the choice or the bias.
+ * Each FP8 GEMM quantises along its contracted dimension: the data
+ * gradients take 1x128 gradient tiles and the forward's 128x128 weight
+ * blocks transposed (moe_transpose_fp8_blocks); the weight gradients take
+ * 128-token x 1-channel tiles of both operands (moe_quant_fp8_128x1_*,
+ * moe_grouped_wgrad_fp8). Order of calls, after a forward whose workspace
+ * is still intact:
+ *   moe_combine_backward -> moe_route_backward -> moe_router_wgrad;
+ *   moe_grouped_gemm_fp8 (dO x W2^T blocks, MOE_EPI_F32) -> dh;
+ *   moe_grouped_gemm_fp8 (x, W13, MOE_EPI_GATEUP_F32) -> a|b;
+ *   moe_swiglu_backward; moe_grouped_gemm_fp8 ([dA|dB] x [W1|W3]^T blocks,
+ *   MOE_EPI_BF16_F32_LAST); moe_dx_combine;
+ *   moe_quant_fp8_128x1_* of dO, h, dA|dB, x; moe_grouped_wgrad_fp8 twice.
+ * All calls: caller-owned device memory, asynchronous on `stream`, host
+ * checks return before any launch, device checks set the status word.
+ * ------------------------------------------------------------------------ */
+
+/* Transposes 128x128-block E4M3 matrices with their scales (a block's codes
+ * and scale carry over exactly):
+ *   q      device u8 [batch][rows][cols], scale f32 [batch][rows/128][cols/128]
+ *   qT     device u8, element (b, c, r) at qT[(b * colsT + c) * ldT + r]
+ *   scaleT device f32, block (b, cb, rb) at scaleT[(b * colsT/128 + cb) * (ldT/128) + rb]
+ * ldT >= rows lets two matrices share the rows of qT, e.g. W1^T and W3^T side
+ * by side as the K order [W1 | W3] of the data gradient of the gate/up
+ * projection; colsT >= cols leaves rows cols .. colsT-1 of each transposed
+ * matrix untouched (zero padding the caller keeps, e.g. to a GEMM's N tile).
+ * rows, cols, ldT, colsT multiples of 128. */
+moe_status moe_transpose_fp8_blocks(const uint8_t* q, const float* scale, int64_t batch, int64_t rows, int64_t cols,
+                                    uint8_t* qT, float* scaleT, int64_t ldT, int64_t colsT, void* stream);
+
+/* Backward of moe_combine for upstream gradient dy (bf16 [T][d]):
+ *   dgate[t][k] = sum_n dy[t][n] * routed_out[row_of[t][k]][n]   (FP32)
+ *   the expert-output gradient of each grouped row, quantised per 1x128 tile
+ *   with scale rule `rule`: row row_of[t][k] holds fl32(topk_gate[t][k] * dy[t]),
+ *   shared row T*K + t holds dy[t]; codes dOq u8 [T*K+T][d], scales dOs
+ *   f32 [T*K+T][d/128];
+ *   row_gate f32 [T*K+T]: the gate of each grouped row (1 for shared rows).
+ * routed_out bf16 [T*K][d] (the forward's routed expert outputs); row_of,
+ * topk_gate as in moe_combine. */
+moe_status moe_combine_backward(const moe_config* cfg, const uint16_t* dy, const uint16_t* routed_out,
+                                const int32_t* row_of, const float* topk_gate, int32_t rule, uint8_t* dOq, float* dOs,
+                                float* row_gate, float* dgate, void* stream);
+
+/* Router logit gradient of the chosen experts: with s_k the affinities the
+ * forward's moe_route computed (recomputed bit for bit from the logits it
+ * left in `workspace`, plus logit_offset if not NULL) and S = sum_k s_k,
+ *   dz[t][k] = (dgate[t][k] - sum_j g_j dgate[t][j]) / S * s_k * (1 - s_k),
+ * g_j = s_j / S. topk_idx, dgate, dz [T][K]. The workspace must be the one
+ * the forward's moe_route used, unchanged since. */
+moe_status moe_route_backward(const moe_config* cfg, const float* logit_offset, const int32_t* topk_idx,
+                              const float* dgate, float* dz, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Router weight gradient: dWr[e][:] = sum over expert e's grouped rows r of
+ * dz[t_r][k_r] * x[t_r][:] (FP32, in row order), with t_r = sorted_token[r]
+ * and k_r the slot with row_of[t_r][k_r] == r. x bf16 [T][d]; offsets
+ * [E+1] and sorted_token, row_of from moe_permute; dWr f32 [E][d] out. */
+moe_status moe_router_wgrad(const moe_config* cfg, const uint16_t* x, const int32_t* offsets,
+                            const int32_t* sorted_token, const int32_t* row_of, const float* dz, float* dWr,
+                            void* stream);
+
+/* SwiGLU backward of h = SiLU(a) * b, SiLU(a) = a * sigmoid(a):
+ *   dA = dh * b * sigmoid(a) * (1 + a * (1 - sigmoid(a))),  dB = dh * SiLU(a).
+ *   ab    f32 [rows][2I] in/out: in, a and b in the MOE_EPI_GATEUP_F32 layout;
+ *         out, dA and dB in the same places
+ *   dh    f32 [rows][ld_dh] (the first I columns are read; ld_dh % 4 == 0)
+ *   dab_q u8 [rows][2I], dab_s f32 [rows][2I/128]: 1x128 E4M3 of [dA | dB]
+ *         (dA in columns [0, I), dB in [I, 2I)) under scale rule `rule`.
+ * I a multiple of 128. */
+moe_status moe_swiglu_backward(int64_t rows, int32_t I, float* ab, const float* dh, int64_t ld_dh, int32_t rule,
+                               uint8_t* dab_q, float* dab_s, void* stream);
+
+/* Input gradient: dx[t] = dx_shared[t] + sum_k (dx_routed[row_of[t][k]] +
+ * dz[t][k] * Wr[topk_idx[t][k]]), FP32 in that order, bf16 result.
+ * dx_routed bf16 [T*K][d], dx_shared f32 [T][d] (the data-gradient GEMM's
+ * MOE_EPI_BF16_F32_LAST outputs), Wr f32 [E][d], dx bf16 [T][d] out. */
+moe_status moe_dx_combine(const moe_config* cfg, const uint16_t* dx_routed, const float* dx_shared,
+                          const int32_t* row_of, const int32_t* topk_idx, const float* dz, const float* Wr, uint16_t* dx,
+                          void* stream);
+
+/* 128x1 grouped quantisation (the 1x128 rule taken along the rows) of a
+ * [rows][cols] operand whose rows are grouped by offsets [groups+1]
+ * (device i32, non-decreasing, offsets[groups] <= rows): group g's rows form
+ * ceil(m_g/128) tiles of 128 rows (the last zero-padded); the s-th tile over
+ * all groups in order becomes columns 128s .. 128s+127 of
+ *   qT device u8 [cols][ldq]   (the codes, transposed: row c = channel c)
+ *   sT device f32 [*][cols]    (scale of tile s, channel c at sT[s * cols + c])
+ * ldq (a multiple of 16) must cover 128 * sum_g ceil(m_g/128), which is at
+ * most 128 * (ceil(rows/128) + groups); a narrower ldq sets
+ * MOE_ERR_DEVICE_CHECK. Padding codes are 0x00. cols a multiple of 128.
+ * The sources differ in where the values come from:
+ *   _f32       v f32 [rows][ld]
+ *   _fp8       fl32(decode(q) * scale) of E4M3 codes q [rows][ld] with 1x128
+ *              scales [rows][ld/128] (ld a multiple of 128): the values an FP8
+ *              GEMM of the forward multiplied
+ *   _bf16_rows fl32(row_mult[r] * x[row_map[r]][:]) of bf16 x [x_rows][ld]
+ *              (row_mult NULL: 1), e.g. the grouped rows of the expert-output
+ *              gradient g * dy. row_map values in [0, x_rows) (else
+ *              MOE_ERR_DEVICE_CHECK and row 0). */
+moe_status moe_quant_fp8_128x1_f32(const float* v, int64_t ld, int32_t groups, const int32_t* offsets, int64_t rows,
+                                   int32_t cols, int32_t rule, uint8_t* qT, int64_t ldq, float* sT, void* stream);
+moe_status moe_quant_fp8_128x1_fp8(const uint8_t* q, const float* scale, int64_t ld, int32_t groups,
+                                   const int32_t* offsets, int64_t rows, int32_t cols, int32_t rule, uint8_t* qT,
+                                   int64_t ldq, float* sT, void* stream);
+moe_status moe_quant_fp8_128x1_bf16_rows(const uint16_t* x, int64_t x_rows, int64_t ld, const int32_t* row_map,
+                                         const float* row_mult, int32_t groups, const int32_t* offsets, int64_t rows,
+                                         int32_t cols, int32_t rule, uint8_t* qT, int64_t ldq, float* sT,
+                                         void* stream);
+
+/* Grouped weight-gradient GEMM on 5th-generation tensor cores: for each group g,
+ *   out[g][m][n] = sum over g's 128-row tiles s of
+ *                  saT[s][m] * sbT[s][n] * sum_{j < 128} AT[m][128s+j] * BT[n][128s+j]
+ * (E4M3 operands from moe_quant_fp8_128x1_*, FP32 promotion per tile), with
+ * g's tiles numbered as moe_quant_fp8_128x1_* numbers them for the same
+ * offsets [groups+1] (device). AT u8 [M][width], BT u8 [N][width], saT f32
+ * [width/128][M], sbT f32 [width/128][N]; out f32 [groups][M][N] (groups
+ * with no rows get zeros). M a multiple of 128, N of 256, width (>= 128 *
+ * sum_g ceil(m_g/128), else MOE_ERR_DEVICE_CHECK) of 128; groups <= 1025;
+ * out 32-byte aligned. */
+moe_status moe_grouped_wgrad_fp8(int32_t groups, const int32_t* offsets, int64_t rows, int64_t width, int32_t M,
+                                 int32_t N, const uint8_t* AT, const float* saT, const uint8_t* BT, const float* sbT,
+                                 float* out, void* stream);
 
 /* Failure-detection self test: launches one kernel that waits, with a
  * limit of `limit_us` microseconds, on a barrier nothing will complete, and

@@ -21,6 +21,7 @@ MOE_EPI_BF16 = 0
 MOE_EPI_SWIGLU_FP8 = 1
 MOE_EPI_F32 = 2
 MOE_EPI_BF16_F32_LAST = 3
+MOE_EPI_GATEUP_F32 = 4
 
 STATUS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE",
@@ -54,6 +55,17 @@ _SIG = {
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_bias_update": (ctypes.c_int, [_I32, _I32, _I32, _P, ctypes.c_float, _P, _P]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
+    "moe_transpose_fp8_blocks": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P, _P, _I64, _I64, _P]),
+    "moe_combine_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P]),
+    "moe_route_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_router_wgrad": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_swiglu_backward": (ctypes.c_int, [_I64, _I32, _P, _P, _I64, _I32, _P, _P, _P]),
+    "moe_dx_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_quant_fp8_128x1_f32": (ctypes.c_int, [_P, _I64, _I32, _P, _I64, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_quant_fp8_128x1_fp8": (ctypes.c_int, [_P, _P, _I64, _I32, _P, _I64, _I32, _I32, _P, _I64, _P, _P]),
+    "moe_quant_fp8_128x1_bf16_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I32, _P, _I64, _I32, _I32, _P, _I64, _P,
+                                                     _P]),
+    "moe_grouped_wgrad_fp8": (ctypes.c_int, [_I32, _P, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -284,7 +296,7 @@ def grouped_gemm_fp8(offsets, A, sa, B, sb, epilogue=MOE_EPI_BF16, out=None, out
         out = torch.empty(rows, N, dtype=torch.bfloat16, device=A.device) if out is None else out
         if out_scale is None:
             out_scale = torch.empty(last_rows, N, dtype=torch.float32, device=A.device)
-    elif epilogue == MOE_EPI_F32:
+    elif epilogue in (MOE_EPI_F32, MOE_EPI_GATEUP_F32):
         out = torch.empty(rows, N, dtype=torch.float32, device=A.device) if out is None else out
     else:
         out = torch.empty(rows, N // 2, dtype=torch.uint8, device=A.device) if out is None else out
@@ -337,3 +349,159 @@ def bias_update(E, T, K, counts, gamma, bias):
     _need(bias, torch.float32, "bias", (E,))
     _call("moe_bias_update", E, T, K, _ptr(counts), ctypes.c_float(gamma), _ptr(bias), _stream())
     return bias
+
+
+# ------------------------------------------------------------------ backward ----
+def transpose_fp8_blocks(q, scale, qT=None, scaleT=None, offset: int = 0):
+    """q u8 [batch][rows][cols], scale f32 [batch][rows/128][cols/128] -> transposed blocks.
+
+    qT u8 [batch][colsT][ldT] and scaleT f32 [batch][colsT/128][ldT/128] (allocated
+    [batch][cols][rows] when None); the source's rows land in columns offset ..
+    offset + rows - 1 of qT (offset a multiple of 128), so two matrices can share
+    qT side by side; rows cols .. colsT-1 of each matrix are left as they are.
+    """
+    _need(q, torch.uint8, "q")
+    b, rows, cols = q.shape
+    _need(scale, torch.float32, "scale", (b, rows // 128, cols // 128))
+    if qT is None:
+        qT = torch.empty(b, cols, rows, dtype=torch.uint8, device=q.device)
+        scaleT = torch.empty(b, cols // 128, rows // 128, dtype=torch.float32, device=q.device)
+    _need(qT, torch.uint8, "qT")
+    _need(scaleT, torch.float32, "scaleT")
+    colsT, ldT = qT.shape[1], qT.shape[2]
+    if qT.shape[0] != b or colsT < cols or offset % 128 or offset + rows > ldT or \
+            tuple(scaleT.shape) != (b, colsT // 128, ldT // 128):
+        raise ValueError("qT / scaleT do not fit the transposed blocks")
+    _call("moe_transpose_fp8_blocks", _ptr(q), _ptr(scale), b, rows, cols, ctypes.c_void_p(qT.data_ptr() + offset),
+          ctypes.c_void_p(scaleT.data_ptr() + 4 * (offset // 128)), ldT, colsT, _stream())
+    return qT, scaleT
+
+
+def combine_backward(cfg, dy, routed_out, row_of, gate, dOq, dOs, row_gate, dgate, rule="fp32"):
+    _need(dy, torch.bfloat16, "dy", (cfg.T, cfg.d))
+    _need(routed_out, torch.bfloat16, "routed_out")
+    if routed_out.shape[0] < cfg.T * cfg.K or routed_out.shape[1] != cfg.d:
+        raise ValueError("routed_out: expected at least T*K rows of d columns")
+    _need(row_of, torch.int32, "row_of", (cfg.T, cfg.K))
+    _need(gate, torch.float32, "topk_gate", (cfg.T, cfg.K))
+    _need(dOq, torch.uint8, "dOq", (cfg.rows, cfg.d))
+    _need(dOs, torch.float32, "dOs", (cfg.rows, cfg.d // 128))
+    _need(row_gate, torch.float32, "row_gate", (cfg.rows,))
+    _need(dgate, torch.float32, "dgate", (cfg.T, cfg.K))
+    c = config_c(cfg)
+    _call("moe_combine_backward", ctypes.byref(c), _ptr(dy), _ptr(routed_out), _ptr(row_of), _ptr(gate), _rule(rule),
+          _ptr(dOq), _ptr(dOs), _ptr(row_gate), _ptr(dgate), _stream())
+
+
+def route_backward(cfg, idx, dgate, workspace, dz, logit_offset=None):
+    _need(idx, torch.int32, "topk_idx", (cfg.T, cfg.K))
+    _need(dgate, torch.float32, "dgate", (cfg.T, cfg.K))
+    _need(dz, torch.float32, "dz", (cfg.T, cfg.K))
+    c = config_c(cfg)
+    _call("moe_route_backward", ctypes.byref(c), _ptr(logit_offset), _ptr(idx), _ptr(dgate), _ptr(dz),
+          _ptr(workspace), workspace.numel(), _stream())
+
+
+def router_wgrad(cfg, x, offsets, sorted_token, row_of, dz, dWr):
+    _need(x, torch.bfloat16, "x", (cfg.T, cfg.d))
+    _need(offsets, torch.int32, "offsets")
+    _need(sorted_token, torch.int32, "sorted_token")
+    _need(row_of, torch.int32, "row_of", (cfg.T, cfg.K))
+    _need(dz, torch.float32, "dz", (cfg.T, cfg.K))
+    _need(dWr, torch.float32, "dWr", (cfg.E, cfg.d))
+    c = config_c(cfg)
+    _call("moe_router_wgrad", ctypes.byref(c), _ptr(x), _ptr(offsets), _ptr(sorted_token), _ptr(row_of), _ptr(dz),
+          _ptr(dWr), _stream())
+
+
+def swiglu_backward(ab, dh, dab_q, dab_s, rule="fp32"):
+    """ab f32 [rows][2I] (a|b in the gate/up tile layout; overwritten by dA|dB), dh f32
+    [rows][>= I] (the first I columns are read)."""
+    _need(ab, torch.float32, "ab")
+    rows, I2 = ab.shape
+    _need(dh, torch.float32, "dh")
+    if dh.shape[0] != rows or dh.shape[1] < I2 // 2:
+        raise ValueError("dh: expected [rows][>= I]")
+    _need(dab_q, torch.uint8, "dab_q", (rows, I2))
+    _need(dab_s, torch.float32, "dab_s", (rows, I2 // 128))
+    _call("moe_swiglu_backward", rows, I2 // 2, _ptr(ab), _ptr(dh), dh.shape[1], _rule(rule), _ptr(dab_q),
+          _ptr(dab_s), _stream())
+
+
+def dx_combine(cfg, dx_routed, dx_shared, row_of, idx, dz, Wr, dx):
+    _need(dx_routed, torch.bfloat16, "dx_routed")
+    if dx_routed.shape[0] < cfg.T * cfg.K or dx_routed.shape[1] != cfg.d:
+        raise ValueError("dx_routed: expected at least T*K rows of d columns")
+    _need(dx_shared, torch.float32, "dx_shared", (cfg.T, cfg.d))
+    _need(row_of, torch.int32, "row_of", (cfg.T, cfg.K))
+    _need(idx, torch.int32, "topk_idx", (cfg.T, cfg.K))
+    _need(dz, torch.float32, "dz", (cfg.T, cfg.K))
+    _need(Wr, torch.float32, "Wr", (cfg.E, cfg.d))
+    _need(dx, torch.bfloat16, "dx", (cfg.T, cfg.d))
+    c = config_c(cfg)
+    _call("moe_dx_combine", ctypes.byref(c), _ptr(dx_routed), _ptr(dx_shared), _ptr(row_of), _ptr(idx), _ptr(dz),
+          _ptr(Wr), _ptr(dx), _stream())
+
+
+def q1_width(groups: int, rows: int) -> int:
+    """Columns a 128x1 grouped operand may need: 128 * (ceil(rows/128) + groups)."""
+    return 128 * ((rows + 127) // 128 + groups)
+
+
+def _q1_out(cols, width, dev, qT, sT):
+    qT = torch.empty(cols, width, dtype=torch.uint8, device=dev) if qT is None else qT
+    sT = torch.empty(width // 128, cols, dtype=torch.float32, device=dev) if sT is None else sT
+    _need(qT, torch.uint8, "qT")
+    _need(sT, torch.float32, "sT")
+    if qT.shape[0] != cols or sT.shape[1] != cols or sT.shape[0] * 128 < qT.shape[1]:
+        raise ValueError("qT [cols][width] and sT [width/128][cols] do not match")
+    return qT, sT
+
+
+def quant_128x1(offsets, rows, cols, rule="fp32", qT=None, sT=None, *, f32=None, fp8=None, bf16_rows=None):
+    """128x1 grouped quantisation of one source (exactly one of):
+      f32=v [rows][cols]; fp8=(q [rows][cols], s [rows][cols/128]);
+      bf16_rows=(x [X][cols], row_map i32 [rows], row_mult f32 [rows] or None).
+    Returns (qT u8 [cols][width], sT f32 [width/128][cols])."""
+    _need(offsets, torch.int32, "offsets")
+    groups = offsets.numel() - 1
+    dev = offsets.device
+    qT, sT = _q1_out(cols, q1_width(groups, rows) if qT is None else qT.shape[1], dev, qT, sT)
+    tail = (groups, _ptr(offsets), rows, cols, _rule(rule), _ptr(qT), qT.shape[1], _ptr(sT), _stream())
+    if f32 is not None:
+        _need(f32, torch.float32, "v")
+        _call("moe_quant_fp8_128x1_f32", _ptr(f32), f32.shape[1], *tail)
+    elif fp8 is not None:
+        q, s = fp8
+        _need(q, torch.uint8, "q")
+        _need(s, torch.float32, "scale", (q.shape[0], q.shape[1] // 128))
+        _call("moe_quant_fp8_128x1_fp8", _ptr(q), _ptr(s), q.shape[1], *tail)
+    else:
+        x, row_map, row_mult = bf16_rows
+        _need(x, torch.bfloat16, "x")
+        _need(row_map, torch.int32, "row_map")
+        if row_mult is not None:
+            _need(row_mult, torch.float32, "row_mult")
+        _call("moe_quant_fp8_128x1_bf16_rows", _ptr(x), x.shape[0], x.shape[1], _ptr(row_map), _ptr(row_mult), *tail)
+    return qT, sT
+
+
+def grouped_wgrad_fp8(offsets, rows, AT, saT, BT, sbT, out=None):
+    """out[g] = AT_g . BT_g^T over group g's 128-row tiles (see moe_grouped_wgrad_fp8)."""
+    _need(offsets, torch.int32, "offsets")
+    groups = offsets.numel() - 1
+    _need(AT, torch.uint8, "AT")
+    _need(BT, torch.uint8, "BT")
+    M, width = AT.shape
+    N = BT.shape[0]
+    if BT.shape[1] != width:
+        raise ValueError("AT and BT must have the same width")
+    _need(saT, torch.float32, "saT")
+    _need(sbT, torch.float32, "sbT")
+    if saT.shape[1] != M or sbT.shape[1] != N or saT.shape[0] * 128 < width or sbT.shape[0] * 128 < width:
+        raise ValueError("scale shapes do not match the operands")
+    out = torch.empty(groups, M, N, dtype=torch.float32, device=AT.device) if out is None else out
+    _need(out, torch.float32, "out", (groups, M, N))
+    _call("moe_grouped_wgrad_fp8", groups, _ptr(offsets), rows, width, M, N, _ptr(AT), _ptr(saT), _ptr(BT), _ptr(sbT),
+          _ptr(out), _stream())
+    return out

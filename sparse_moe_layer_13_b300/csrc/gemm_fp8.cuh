@@ -140,10 +140,11 @@ __device__ __forceinline__ bool store_tile(float* acc, const Params& p, SmemT& s
     const int g = t.g, nt = t.nt;
     const bool valid = rit < t.m_valid;
     const int64_t row = static_cast<int64_t>(t.row0) + rit;
-        const bool f32_out = (EPI == MOE_EPI_F32) || (EPI == MOE_EPI_BF16_F32_LAST && g == groups - 1);
+        const bool f32_out = (EPI == MOE_EPI_F32) || (EPI == MOE_EPI_GATEUP_F32) ||
+                             (EPI == MOE_EPI_BF16_F32_LAST && g == groups - 1);
         if (f32_out) {
             if (valid) {
-                float* dst = (EPI == MOE_EPI_F32)
+                float* dst = (EPI != MOE_EPI_BF16_F32_LAST)
                                  ? static_cast<float*>(p.out) + row * p.N + nt * BN + half * 128
                                  : p.out_aux + (row - last_start) * p.N + nt * BN + half * 128;
 #pragma unroll
@@ -373,6 +374,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         // flight while the previous tile finishes; with fewer than three K chunks it would
         // have to skip tiles, so each tile then starts its own copies.
         struct ScaleRows { uint32_t sa; uint32_t sb; };   // element offsets of a tile's scale rows
+        constexpr bool kSwigluLayout = EPI == MOE_EPI_SWIGLU_FP8 || EPI == MOE_EPI_GATEUP_F32;
         auto scale_rows = [&](const TileInfo& t) {
             const int g = t.g, nt = t.nt;
             int64_t src_row = rit < t.m_valid ? static_cast<int64_t>(t.row0) + rit : 0;
@@ -380,9 +382,9 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 src_row = __ldg(p.row_index + src_row);
                 if (src_row < 0 || src_row >= p.a_rows) src_row = 0;      // reported by the producer
             }
-            // weight scale rows: SwiGLU -> gate block 2*nt (up block 2*nt+1 is nkc further on);
+            // weight scale rows: SwiGLU layout -> gate block 2*nt (up block 2*nt+1 is nkc further on);
             // otherwise block 2*nt+half. Offsets stay below 2^32 (checked at launch).
-            const int64_t sb0 = (static_cast<int64_t>(g) * nbn + 2 * nt + (EPI == MOE_EPI_SWIGLU_FP8 ? 0 : half)) * nkc;
+            const int64_t sb0 = (static_cast<int64_t>(g) * nbn + 2 * nt + (kSwigluLayout ? 0 : half)) * nkc;
             return ScaleRows{static_cast<uint32_t>(src_row * nkc), static_cast<uint32_t>(sb0)};
         };
         // copies the scales of K chunk kc of the tile at `rows` into ring slot `slot`, as one group
@@ -390,7 +392,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             cp_async_4(&s.ring_sa[slot][et], p.sa + rows.sa + kc);
             if (lane == 0) {
                 cp_async_4(&s.ring_sb[slot][ew][0], p.sb + rows.sb + kc);
-                cp_async_4(&s.ring_sb[slot][ew][1], p.sb + rows.sb + (EPI == MOE_EPI_SWIGLU_FP8 ? nkc : 0) + kc);
+                cp_async_4(&s.ring_sb[slot][ew][1], p.sb + rows.sb + (kSwigluLayout ? nkc : 0) + kc);
             }
         };
         // hands chunk buffer b back to the MMA issuer once this warp's loads from it have
@@ -401,7 +403,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             if (lane == 0) mbar_arrive(&s.tempty[b]);
         };
         // (the all-FP32 store epilogue keeps per-tile copies: the look-ahead state makes it spill)
-        const bool ahead = EPI != MOE_EPI_F32 && nkc >= 3;
+        const bool ahead = EPI != MOE_EPI_F32 && EPI != MOE_EPI_GATEUP_F32 && nkc >= 3;
         uint32_t it = 0, tcount = 0;
         bool ok = true;
         ScaleRows cur{0, 0}, nxt{0, 0};

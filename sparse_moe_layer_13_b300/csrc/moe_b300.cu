@@ -5,8 +5,10 @@
 
 #include <mutex>
 
+#include "backward.cuh"
 #include "common.cuh"
 #include "gemm_fp8.cuh"
+#include "gemm_wgrad.cuh"
 #include "gemm_mx.cuh"
 #include "misc.cuh"
 #include "permute.cuh"
@@ -179,6 +181,7 @@ moe_status launch_gemm_epi(int32_t epilogue, const CUtensorMap& ta, const CUtens
     if (epilogue == MOE_EPI_BF16) return launch_gemm<MOE_EPI_BF16, GATHER>(ta, tb, p, tiles_max, st);
     if (epilogue == MOE_EPI_F32) return launch_gemm<MOE_EPI_F32, GATHER>(ta, tb, p, tiles_max, st);
     if (epilogue == MOE_EPI_BF16_F32_LAST) return launch_gemm<MOE_EPI_BF16_F32_LAST, GATHER>(ta, tb, p, tiles_max, st);
+    if (epilogue == MOE_EPI_GATEUP_F32) return launch_gemm<MOE_EPI_GATEUP_F32, GATHER>(ta, tb, p, tiles_max, st);
     return launch_gemm<MOE_EPI_SWIGLU_FP8, GATHER>(ta, tb, p, tiles_max, st);
 }
 
@@ -205,8 +208,9 @@ moe_status grouped_gemm(int32_t groups, const int32_t* offsets, int64_t rows, in
     if (!offsets || !A || !sa || !B || !sb || !out || rows < 0 || a_rows < 0 || groups < 1 || N < 0 || Kdim < 0)
         return MOE_ERR_INVALID_ARG;
     if (epilogue != MOE_EPI_BF16 && epilogue != MOE_EPI_SWIGLU_FP8 && epilogue != MOE_EPI_F32 &&
-        epilogue != MOE_EPI_BF16_F32_LAST)
+        epilogue != MOE_EPI_BF16_F32_LAST && epilogue != MOE_EPI_GATEUP_F32)
         return MOE_ERR_INVALID_ARG;
+    if (epilogue == MOE_EPI_GATEUP_F32 && block_scaled) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((epilogue == MOE_EPI_SWIGLU_FP8 || epilogue == MOE_EPI_BF16_F32_LAST) && !out_aux) return MOE_ERR_INVALID_ARG;
     if (epilogue == MOE_EPI_BF16_F32_LAST && !aligned16(out_aux)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
@@ -286,6 +290,40 @@ void launch_balance_partial(const float* z, int ks, const moe_config* c, const f
     const int nchunk = c->T / 32;
     const int grid = static_cast<int>(std::min<int64_t>(ceil_div(nchunk, 4), static_cast<int64_t>(num_sms()) * 8));
     route::balance_partial_kernel<EPL><<<grid, 128, 0, st>>>(z, ks, c->T, c->E, c->K, offset, idx, p_part, c_part);
+}
+
+// Checks shared by the 128x1 grouped quantisers; returns MOE_OK to launch.
+moe_status check_q1(int32_t groups, const int32_t* offsets, int64_t rows, int32_t cols, int32_t rule,
+                    const uint8_t* qT, int64_t ldq, const float* sT) {
+    if (!offsets || !qT || !sT || groups < 1 || rows < 0 || cols < 0 || ldq < 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(qT) || !aligned16(sT) || ldq % 16) return MOE_ERR_INVALID_ARG;
+    if (rule != MOE_SCALE_FP32 && rule != MOE_SCALE_POW2) return MOE_ERR_INVALID_ARG;
+    if (groups > bwd::kQ1MaxGroups || cols % 128 || rows >= INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+template <int SRC>
+moe_status launch_q1(const bwd::QSrc& src, int32_t groups, const int32_t* offsets, int64_t rows, int32_t cols,
+                     int32_t rule, uint8_t* qT, int64_t ldq, float* sT, cudaStream_t st) {
+    if (rows == 0 || cols == 0) return MOE_OK;
+    const size_t smem = 128 * 129 * sizeof(float) + static_cast<size_t>(groups + 1) * sizeof(int);
+    static bool attr_set[2] = {false, false};
+    const int ri = rule == MOE_SCALE_POW2 ? 1 : 0;
+    if (!attr_set[ri]) {
+        const void* fn = rule == MOE_SCALE_POW2 ? reinterpret_cast<const void*>(bwd::quant_128x1_kernel<SRC, true>)
+                                                : reinterpret_cast<const void*>(bwd::quant_128x1_kernel<SRC, false>);
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(128 * 129 * sizeof(float) + (bwd::kQ1MaxGroups + 1) * sizeof(int))) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set[ri] = true;
+    }
+    const dim3 grid(static_cast<unsigned>(ceil_div(rows, 128) + groups), static_cast<unsigned>(cols / 128));
+    if (rule == MOE_SCALE_POW2)
+        bwd::quant_128x1_kernel<SRC, true><<<grid, 256, smem, st>>>(src, rows, cols, groups, offsets, qT, ldq, sT);
+    else
+        bwd::quant_128x1_kernel<SRC, false><<<grid, 256, smem, st>>>(src, rows, cols, groups, offsets, qT, ldq, sT);
+    return launch_status();
 }
 
 }  // namespace
@@ -586,6 +624,163 @@ moe_status moe_bias_update(int32_t E, int32_t T, int32_t K, const int32_t* count
     if (!counts || !bias || E < 1 || T < 0 || K < 1) return MOE_ERR_INVALID_ARG;
     bias_update_kernel<<<static_cast<unsigned>(ceil_div(E, 256)), 256, 0, as_stream(stream)>>>(E, T, K, counts, gamma,
                                                                                               bias);
+    return launch_status();
+}
+
+// ------------------------------------------------------------- backward ----
+moe_status moe_transpose_fp8_blocks(const uint8_t* q, const float* scale, int64_t batch, int64_t rows, int64_t cols,
+                                    uint8_t* qT, float* scaleT, int64_t ldT, int64_t colsT, void* stream) {
+    if (!q || !scale || !qT || !scaleT || batch < 0 || rows < 0 || cols < 0 || ldT < rows || colsT < cols)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(qT) || ldT % 16) return MOE_ERR_INVALID_ARG;
+    if (rows % 128 || cols % 128 || ldT % 128 || colsT % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int64_t blocks = batch * (rows / 128) * (cols / 128);
+    if (blocks == 0) return MOE_OK;
+    if (blocks > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    bwd::transpose_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, as_stream(stream)>>>(q, scale, rows, cols, qT,
+                                                                                              scaleT, ldT, colsT);
+    return launch_status();
+}
+
+moe_status moe_combine_backward(const moe_config* cfg, const uint16_t* dy, const uint16_t* routed_out,
+                                const int32_t* row_of, const float* topk_gate, int32_t rule, uint8_t* dOq, float* dOs,
+                                float* row_gate, float* dgate, void* stream) {
+    if (const moe_status cs = check_config(cfg); cs != MOE_OK) return cs;
+    if (!dy || !routed_out || !row_of || !topk_gate || !dOq || !dOs || !row_gate || !dgate) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(routed_out) || !aligned16(dOq)) return MOE_ERR_INVALID_ARG;
+    if (rule != MOE_SCALE_FP32 && rule != MOE_SCALE_POW2) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    if (rule == MOE_SCALE_POW2)
+        bwd::combine_backward_kernel<true><<<cfg->T, 256, 0, st>>>(dy, routed_out, row_of, topk_gate, cfg->T, cfg->K,
+                                                                   cfg->d, dOq, dOs, row_gate, dgate);
+    else
+        bwd::combine_backward_kernel<false><<<cfg->T, 256, 0, st>>>(dy, routed_out, row_of, topk_gate, cfg->T, cfg->K,
+                                                                    cfg->d, dOq, dOs, row_gate, dgate);
+    return launch_status();
+}
+
+moe_status moe_route_backward(const moe_config* cfg, const float* logit_offset, const int32_t* topk_idx,
+                              const float* dgate, float* dz, void* workspace, size_t workspace_bytes, void* stream) {
+    if (const moe_status cs = check_config(cfg); cs != MOE_OK) return cs;
+    if (!topk_idx || !dgate || !dz) return MOE_ERR_INVALID_ARG;
+    const WsLayout wl = ws_layout(cfg);
+    if (workspace == nullptr || workspace_bytes < wl.total) return MOE_ERR_WORKSPACE;
+    const float* z = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + wl.logits);
+    bwd::route_backward_kernel<<<static_cast<unsigned>(ceil_div(cfg->T, 4)), 128, 0, as_stream(stream)>>>(
+        z, route_ksplit(cfg), cfg->T, cfg->E, cfg->K, logit_offset, topk_idx, dgate, dz);
+    return launch_status();
+}
+
+moe_status moe_router_wgrad(const moe_config* cfg, const uint16_t* x, const int32_t* offsets,
+                            const int32_t* sorted_token, const int32_t* row_of, const float* dz, float* dWr,
+                            void* stream) {
+    if (const moe_status cs = check_config(cfg); cs != MOE_OK) return cs;
+    if (!x || !offsets || !sorted_token || !row_of || !dz || !dWr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(dWr)) return MOE_ERR_INVALID_ARG;
+    const dim3 grid(static_cast<unsigned>(cfg->E), static_cast<unsigned>(ceil_div(cfg->d, 512)));
+    bwd::router_wgrad_kernel<<<grid, 256, 0, as_stream(stream)>>>(x, cfg->T, cfg->K, cfg->d, offsets, sorted_token,
+                                                                  row_of, dz, dWr);
+    return launch_status();
+}
+
+moe_status moe_swiglu_backward(int64_t rows, int32_t I, float* ab, const float* dh, int64_t ld_dh, int32_t rule,
+                               uint8_t* dab_q, float* dab_s, void* stream) {
+    if (!ab || !dh || !dab_q || !dab_s || rows < 0 || I < 0 || ld_dh < I) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ab) || !aligned16(dh) || !aligned16(dab_q) || ld_dh % 4) return MOE_ERR_INVALID_ARG;
+    if (rule != MOE_SCALE_FP32 && rule != MOE_SCALE_POW2) return MOE_ERR_INVALID_ARG;
+    if (I % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0 || I == 0) return MOE_OK;
+    const int64_t warps = rows * (I / 128);
+    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(warps, 8), static_cast<int64_t>(num_sms()) * 32));
+    if (rule == MOE_SCALE_POW2)
+        bwd::swiglu_backward_kernel<true><<<grid, 256, 0, as_stream(stream)>>>(ab, dh, ld_dh, rows, I, dab_q, dab_s);
+    else
+        bwd::swiglu_backward_kernel<false><<<grid, 256, 0, as_stream(stream)>>>(ab, dh, ld_dh, rows, I, dab_q, dab_s);
+    return launch_status();
+}
+
+moe_status moe_dx_combine(const moe_config* cfg, const uint16_t* dx_routed, const float* dx_shared,
+                          const int32_t* row_of, const int32_t* topk_idx, const float* dz, const float* Wr, uint16_t* dx,
+                          void* stream) {
+    if (const moe_status cs = check_config(cfg); cs != MOE_OK) return cs;
+    if (!dx_routed || !dx_shared || !row_of || !topk_idx || !dz || !Wr || !dx) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dx_routed) || !aligned16(dx_shared) || !aligned16(Wr) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
+    bwd::dx_combine_kernel<<<cfg->T, 256, 0, as_stream(stream)>>>(dx_routed, dx_shared, row_of, topk_idx, dz, Wr,
+                                                                 cfg->T, cfg->K, cfg->d, cfg->E, dx);
+    return launch_status();
+}
+
+moe_status moe_quant_fp8_128x1_f32(const float* v, int64_t ld, int32_t groups, const int32_t* offsets, int64_t rows,
+                                   int32_t cols, int32_t rule, uint8_t* qT, int64_t ldq, float* sT, void* stream) {
+    if (const moe_status cs = check_q1(groups, offsets, rows, cols, rule, qT, ldq, sT); cs != MOE_OK) return cs;
+    if (!v || !aligned16(v) || ld < cols || ld % 4) return MOE_ERR_INVALID_ARG;
+    bwd::QSrc src{};
+    src.f32 = v;
+    src.ld = ld;
+    return launch_q1<bwd::SRC_F32>(src, groups, offsets, rows, cols, rule, qT, ldq, sT, as_stream(stream));
+}
+
+moe_status moe_quant_fp8_128x1_fp8(const uint8_t* q, const float* scale, int64_t ld, int32_t groups,
+                                   const int32_t* offsets, int64_t rows, int32_t cols, int32_t rule, uint8_t* qT,
+                                   int64_t ldq, float* sT, void* stream) {
+    if (const moe_status cs = check_q1(groups, offsets, rows, cols, rule, qT, ldq, sT); cs != MOE_OK) return cs;
+    if (!q || !scale || !aligned16(q) || ld < cols || ld % 128) return MOE_ERR_INVALID_ARG;
+    bwd::QSrc src{};
+    src.q8 = q;
+    src.s8 = scale;
+    src.ld = ld;
+    src.ld_s = ld / 128;
+    return launch_q1<bwd::SRC_FP8>(src, groups, offsets, rows, cols, rule, qT, ldq, sT, as_stream(stream));
+}
+
+moe_status moe_quant_fp8_128x1_bf16_rows(const uint16_t* x, int64_t x_rows, int64_t ld, const int32_t* row_map,
+                                         const float* row_mult, int32_t groups, const int32_t* offsets, int64_t rows,
+                                         int32_t cols, int32_t rule, uint8_t* qT, int64_t ldq, float* sT,
+                                         void* stream) {
+    if (const moe_status cs = check_q1(groups, offsets, rows, cols, rule, qT, ldq, sT); cs != MOE_OK) return cs;
+    if (!x || !row_map || !aligned16(x) || ld < cols || ld % 8 || x_rows < 0) return MOE_ERR_INVALID_ARG;
+    bwd::QSrc src{};
+    src.bf16 = x;
+    src.map = row_map;
+    src.mult = row_mult;
+    src.ld = ld;
+    src.src_rows = x_rows;
+    return launch_q1<bwd::SRC_BF16_ROWS>(src, groups, offsets, rows, cols, rule, qT, ldq, sT, as_stream(stream));
+}
+
+moe_status moe_grouped_wgrad_fp8(int32_t groups, const int32_t* offsets, int64_t rows, int64_t width, int32_t M,
+                                 int32_t N, const uint8_t* AT, const float* saT, const uint8_t* BT, const float* sbT,
+                                 float* out, void* stream) {
+    if (!offsets || !AT || !saT || !BT || !sbT || !out || groups < 1 || rows < 0 || width < 0 || M < 0 || N < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(AT) || !aligned16(BT) || !aligned16(saT) || !aligned16(sbT) ||
+        (reinterpret_cast<uintptr_t>(out) & 31u) != 0)      // 32-byte vector stores
+        return MOE_ERR_INVALID_ARG;
+    if (groups > wgrad::MAX_GROUPS || M % gemm::BM || N % gemm::BN || width % 128 || M == 0 || N == 0 ||
+        rows >= INT32_MAX || width >= INT32_MAX)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(groups) * (M / gemm::BM) * (N / gemm::BN) >= INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (width == 0) {
+        // no rows at all: every gradient is zero
+        return cudaMemsetAsync(out, 0, static_cast<size_t>(groups) * M * N * sizeof(float), as_stream(stream)) ==
+                       cudaSuccess
+                   ? MOE_OK
+                   : MOE_ERR_CUDA;
+    }
+    CUtensorMap ta, tb;
+    if (!make_map_u8(&ta, AT, static_cast<uint64_t>(width), static_cast<uint64_t>(M), gemm::BM)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&tb, BT, static_cast<uint64_t>(width), static_cast<uint64_t>(N), gemm::BN)) return MOE_ERR_CUDA;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(wgrad::grouped_wgrad_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(wgrad::SMEM_BYTES)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr_set = true;
+    }
+    wgrad::Params p{offsets, groups, rows, width / 128, M, N, saT, sbT, out};
+    const int64_t tiles = static_cast<int64_t>(groups) * (M / gemm::BM) * (N / gemm::BN);
+    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), tiles));
+    wgrad::grouped_wgrad_fp8_kernel<<<grid, gemm::NUM_THREADS, wgrad::SMEM_BYTES, as_stream(stream)>>>(ta, tb, p);
     return launch_status();
 }
 

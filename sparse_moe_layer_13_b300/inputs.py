@@ -11,6 +11,7 @@ Recipe (all draws from ``torch.Generator`` seeded per tensor):
 * bias    : fp32 [E], zeros or U(-0.1, 0.1).
 * W1, W3  : fp32 [I][d] per expert, N(0, 1/d) (gate and up projections).
 * W2      : fp32 [d][I] per expert, N(0, 1/d) (down projection).
+* dy      : bf16 [T][d], N(0, 1), the upstream gradient of a backward pass.
 * logit offsets (skewed workload only): o_e = -c * s * ln(rank_e) with rank a
   seeded permutation of 1..E, giving a Zipf(s)-shaped expert popularity.
 
@@ -27,7 +28,7 @@ import torch
 
 from .configs import MoEConfig
 
-_TAG = {"x": 1, "router": 2, "bias": 3, "w1": 4, "w3": 5, "w2": 6, "rank": 7}
+_TAG = {"x": 1, "router": 2, "bias": 3, "w1": 4, "w3": 5, "w2": 6, "rank": 7, "dy": 8}
 
 
 def _gen(cfg_seed: int, tag: str, idx: int, device) -> torch.Generator:
@@ -40,6 +41,11 @@ def gen_x(cfg: MoEConfig, device="cpu", step: int = 0, T: int | None = None) -> 
     T = cfg.T if T is None else T
     g = _gen(cfg.seed, "x", step, device)
     return torch.randn(T, cfg.d, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def gen_dy(cfg: MoEConfig, device="cpu", step: int = 0) -> torch.Tensor:
+    g = _gen(cfg.seed, "dy", step, device)
+    return torch.randn(cfg.T, cfg.d, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
 def gen_router(cfg: MoEConfig, device="cpu") -> torch.Tensor:

@@ -34,15 +34,27 @@ class ExpertWeights:
 
     q13 u8 [E+1][2I][d] (SwiGLU layout), s13 f32 [E+1][2I/128][d/128],
     q2  u8 [E+1][d][I],                  s2  f32 [E+1][d/128][I/128].
+    With backward=True also the transposed blocks the data gradients use:
+    q13T u8 [E+1][d][2I] (K order [W1 | W3]), s13T f32 [E+1][d/128][2I/128],
+    q2T  u8 [E+1][Ip][d] (rows I..Ip-1 zero, Ip = I rounded up to 256),
+                         s2T f32 [E+1][Ip/128][d/128].
     """
 
-    def __init__(self, cfg: MoEConfig, device="cuda", chunk: int = 16, scale_rule: str = "fp32"):
+    def __init__(self, cfg: MoEConfig, device="cuda", chunk: int = 16, scale_rule: str = "fp32",
+                 backward: bool = False):
         E1, I, d = cfg.E + 1, cfg.I, cfg.d
         self.scale_rule = scale_rule
+        self.backward = backward
         self.q13 = torch.empty(E1, 2 * I, d, dtype=torch.uint8, device=device)
         self.s13 = torch.empty(E1, 2 * I // 128, d // 128, dtype=torch.float32, device=device)
         self.q2 = torch.empty(E1, d, I, dtype=torch.uint8, device=device)
         self.s2 = torch.empty(E1, d // 128, I // 128, dtype=torch.float32, device=device)
+        if backward:
+            Ip = (I + 255) // 256 * 256
+            self.q13T = torch.empty(E1, d, 2 * I, dtype=torch.uint8, device=device)
+            self.s13T = torch.empty(E1, d // 128, 2 * I // 128, dtype=torch.float32, device=device)
+            self.q2T = torch.zeros(E1, Ip, d, dtype=torch.uint8, device=device)
+            self.s2T = torch.zeros(E1, Ip // 128, d // 128, dtype=torch.float32, device=device)
         for e0 in range(0, E1, chunk):
             e1 = min(E1, e0 + chunk)
             ws = [inputs.gen_expert(cfg, e, device) for e in range(e0, e1)]
@@ -54,6 +66,10 @@ class ExpertWeights:
             q3, s3 = B.quant_128x128(w3, rule=scale_rule)
             B.pack_w13(q1, s1, q3, s3, self.q13[e0:e1], self.s13[e0:e1])
             B.quant_128x128(w2, self.q2[e0:e1], self.s2[e0:e1], rule=scale_rule)
+            if backward:
+                B.transpose_fp8_blocks(q1, s1, self.q13T[e0:e1], self.s13T[e0:e1], offset=0)
+                B.transpose_fp8_blocks(q3, s3, self.q13T[e0:e1], self.s13T[e0:e1], offset=I)
+                B.transpose_fp8_blocks(self.q2[e0:e1], self.s2[e0:e1], self.q2T[e0:e1], self.s2T[e0:e1])
             del w1, w3, w2, q1, q3
 
 
@@ -61,7 +77,8 @@ class MoELayer:
     """One layer instance: router weight, selection bias, expert weights, buffers."""
 
     def __init__(self, cfg: MoEConfig, device="cuda", weights: ExpertWeights | None = None,
-                 logit_offset: torch.Tensor | None = None, token_rows: str = "scatter", scale_rule: str = "fp32"):
+                 logit_offset: torch.Tensor | None = None, token_rows: str = "scatter", scale_rule: str = "fp32",
+                 backward: bool = False):
         if token_rows not in ("scatter", "copy", "gather"):
             raise ValueError(f"token_rows: {token_rows!r}")
         if scale_rule not in ("fp32", "pow2"):
@@ -76,7 +93,8 @@ class MoELayer:
         self.Wr = inputs.gen_router(cfg, device)
         self.bias = inputs.gen_bias(cfg, device)
         self.logit_offset = logit_offset
-        self.w = ExpertWeights(cfg, device, scale_rule=scale_rule) if weights is None else weights
+        self.w = ExpertWeights(cfg, device, scale_rule=scale_rule, backward=backward) if weights is None else weights
+        self._bwd = None
         if self.w.scale_rule != scale_rule:
             raise ValueError("the expert weights were quantised with another scale rule")
         T, K, E, d, I = cfg.T, cfg.K, cfg.E, cfg.d, cfg.I
@@ -147,6 +165,78 @@ class MoELayer:
                 counts_hook(self.counts)
             B.bias_update(c.E, c.T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
         return y
+
+    def backward(self, x: torch.Tensor, dy: torch.Tensor) -> dict:
+        """Gradients of the last forward (on x) for upstream gradient dy (bf16 [T][d]),
+        with the chosen experts held fixed, on the current stream.
+
+        Reads what the forward left: routing, grouped rows, the quantised x and
+        h, the routed outputs and the router logits in the workspace; call it
+        before the next forward. Needs weights built with backward=True and
+        token_rows "scatter" or "copy". Returns device tensors (reused by the
+        next call):
+          dx   bf16 [T][d]
+          dWr  f32  [E][d]
+          dW13 f32  [E+1][2I][d]  in the q13 (SwiGLU tile) row layout
+          dW2T f32  [E+1][I][d]   the down projection's gradient, transposed
+          dgate, dz f32 [T][K]    gate and router-logit gradients
+        Every FP8 GEMM runs on the FP32-scale tensor-core kernels under the
+        layer's scale rule.
+        """
+        c = self.cfg
+        if not getattr(self.w, "backward", False):
+            raise ValueError("expert weights were built without backward=True")
+        if self.token_rows == "gather":
+            raise ValueError("the backward pass reads the grouped token rows; use token_rows 'scatter' or 'copy'")
+        B._need(dy, torch.bfloat16, "dy", (c.T, c.d))
+        bw = self._bwd_buffers()
+        rule = self.scale_rule
+        T, K, E, d, I = c.T, c.K, c.E, c.d, c.I
+        R = c.rows
+        offs, st, ro = self.perm["offsets"], self.perm["sorted_token"], self.perm["row_of"]
+        B.combine_backward(c, dy, self.out, ro, self.gate, bw["dOq"], bw["dOs"], bw["row_gate"], bw["dgate"], rule)
+        B.route_backward(c, self.idx, bw["dgate"], self.ws, bw["dz"], self.logit_offset)
+        B.router_wgrad(c, x, offs[:E + 1], st, ro, bw["dz"], bw["dWr"])
+        B.grouped_gemm_fp8(offs, bw["dOq"], bw["dOs"], self.w.q2T, self.w.s2T, B.MOE_EPI_F32, bw["dh"])
+        B.grouped_gemm_fp8(offs, self.xq_perm, self.xs_perm, self.w.q13, self.w.s13, B.MOE_EPI_GATEUP_F32, bw["ab"])
+        B.swiglu_backward(bw["ab"], bw["dh"], bw["dabq"], bw["dabs"], rule)
+        B.grouped_gemm_fp8(offs, bw["dabq"], bw["dabs"], self.w.q13T, self.w.s13T, B.MOE_EPI_BF16_F32_LAST,
+                           bw["dxr"], bw["dxs"])
+        B.dx_combine(c, bw["dxr"], bw["dxs"], ro, self.idx, bw["dz"], self.Wr, bw["dx"])
+        B.quant_128x1(offs, R, d, rule, bw["oT"], bw["oS"], bf16_rows=(dy, st, bw["row_gate"]))
+        B.quant_128x1(offs, R, I, rule, bw["hT"], bw["hS"], fp8=(self.hq, self.hs))
+        B.quant_128x1(offs, R, 2 * I, rule, bw["gT"], bw["gS"], f32=bw["ab"])
+        B.quant_128x1(offs, R, d, rule, bw["xT"], bw["xS"], fp8=(self.xq_perm, self.xs_perm))
+        B.grouped_wgrad_fp8(offs, R, bw["hT"], bw["hS"], bw["oT"], bw["oS"], bw["dW2T"])
+        B.grouped_wgrad_fp8(offs, R, bw["gT"], bw["gS"], bw["xT"], bw["xS"], bw["dW13"])
+        return {k: bw[k] for k in ("dx", "dWr", "dW13", "dW2T", "dgate", "dz")}
+
+    # library kernel launches per backward: combine 1, route 1, router weight 1, GEMMs 5,
+    # SwiGLU 1, input gradient 1, 128x1 quantisers 4
+    launches_per_backward = 14
+
+    def _bwd_buffers(self) -> dict:
+        if getattr(self, "_bwd", None) is None:
+            c = self.cfg
+            T, K, E, d, I = c.T, c.K, c.E, c.d, c.I
+            R = c.rows
+            Ip = self.w.q2T.shape[1]
+            W = B.q1_width(E + 1, R)
+            z = lambda *s, dt: torch.empty(*s, dtype=dt, device=self.device)  # noqa: E731
+            f32, u8 = torch.float32, torch.uint8
+            self._bwd = {
+                "dOq": z(R, d, dt=u8), "dOs": z(R, d // 128, dt=f32), "row_gate": z(R, dt=f32),
+                "dgate": z(T, K, dt=f32), "dz": z(T, K, dt=f32), "dWr": z(E, d, dt=f32),
+                "dh": z(R, Ip, dt=f32), "ab": z(R, 2 * I, dt=f32),
+                "dabq": z(R, 2 * I, dt=u8), "dabs": z(R, 2 * I // 128, dt=f32),
+                "dxr": z(R, d, dt=torch.bfloat16), "dxs": z(T, d, dt=f32), "dx": z(T, d, dt=torch.bfloat16),
+                "oT": z(d, W, dt=u8), "oS": z(W // 128, d, dt=f32),
+                "hT": z(I, W, dt=u8), "hS": z(W // 128, I, dt=f32),
+                "gT": z(2 * I, W, dt=u8), "gS": z(W // 128, 2 * I, dt=f32),
+                "xT": z(d, W, dt=u8), "xS": z(W // 128, d, dt=f32),
+                "dW2T": z(E + 1, I, d, dt=f32), "dW13": z(E + 1, 2 * I, d, dt=f32),
+            }
+        return self._bwd
 
     def balance_loss(self, seq_len: int, alpha: float, stats: bool = False):
         """Sequence-wise balance loss of the last forward's routing (loss per sequence of

@@ -1,0 +1,315 @@
+"""GPU parity of the backward pass against the FP64 oracle (oracle/backward.py).
+
+Kernel by kernel on seeded synthetic operands (bit-exact for E4M3 codes,
+scales and transposed bytes; FP32 tolerances for sums), then the whole
+layer backward on the workload shapes: every gradient at tiny size, sampled
+tokens and experts at mid and full width.
+
+Tolerances for the layer gradients are the layer output's (relative L2
+<= 5e-3, max |diff| <= 2e-2 * RMS): the backward GEMMs quantise to E4M3 at
+the same kind of points as the forward, and each gradient is one more chain
+of FP8 GEMMs with FP32 promotion.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_y_close, gpu, oracle_experts, require_gpu, to_np
+from oracle import e4m3
+from oracle.backward import (Quantiser, dequant_expert, gemm_fp8_wgrad, layer_backward, quant_128x1_grouped,
+                             segment_starts, swiglu_grad)
+from oracle.quant import quant_1x128
+from oracle.route import affinity, near_tie, route as oracle_route
+from sparse_moe_layer_13_b300.configs import CONFIGS
+
+SIZES = [0, 5, 130, 128, 1, 0, 257, 384]
+
+
+def _offsets(sizes):
+    return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+
+
+def _codes(rng, shape):
+    """Seeded finite E4M3 codes (no NaN)."""
+    c = rng.integers(0, 256, shape).astype(np.uint8)
+    return np.where((c & 0x7F) == 0x7F, c ^ 0x01, c).astype(np.uint8)
+
+
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
+
+
+def _check_q1(B, offs, qT, sT, want_q, want_s):
+    P = segment_starts(offs)
+    width = int(P[-1])
+    assert np.array_equal(to_np(qT)[:, :width], want_q), "128x1 codes differ"
+    got_s = to_np(sT)[:width // 128]
+    assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32)), "128x1 scales differ"
+
+
+@gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
+def test_quant_128x1_f32_source(rule):
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding as B
+    rng = np.random.default_rng(10)
+    offs = _offsets(SIZES)
+    R, C = int(offs[-1]) + 3, 384                      # three trailing rows outside every group
+    v = (rng.standard_normal((R, C)) * np.exp(rng.uniform(-6, 6, (R, C)))).astype(np.float32)
+    v[7:20, 5] = 0.0
+    qT, sT = B.quant_128x1(torch.from_numpy(offs).cuda(), R, C, rule, f32=torch.from_numpy(v).cuda())
+    want_q, want_s = quant_128x1_grouped(v, offs, rule)
+    _check_q1(B, offs, qT, sT, want_q, want_s)
+
+
+@gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
+def test_quant_128x1_fp8_source(rule):
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding as B
+    rng = np.random.default_rng(11)
+    offs = _offsets(SIZES)
+    R, C = int(offs[-1]), 256
+    q = _codes(rng, (R, C))
+    s = rng.uniform(1e-3, 4.0, (R, C // 128)).astype(np.float32)
+    qT, sT = B.quant_128x1(torch.from_numpy(offs).cuda(), R, C, rule,
+                           fp8=(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()))
+    vals = (e4m3.decode(q).reshape(R, C // 128, 128) * s.astype(np.float64)[:, :, None]).reshape(R, C)
+    want_q, want_s = quant_128x1_grouped(vals.astype(np.float32), offs, rule)
+    _check_q1(B, offs, qT, sT, want_q, want_s)
+
+
+@gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
+def test_quant_128x1_bf16_rows_source(rule):
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding as B
+    rng = np.random.default_rng(12)
+    offs = _offsets(SIZES)
+    R, C, X = int(offs[-1]), 256, 300
+    x = _bf16(rng.standard_normal((X, C)) * 3)
+    row_map = rng.integers(0, X, R).astype(np.int32)
+    mult = rng.uniform(0.01, 1.0, R).astype(np.float32)
+    qT, sT = B.quant_128x1(torch.from_numpy(offs).cuda(), R, C, rule,
+                           bf16_rows=(x.cuda(), torch.from_numpy(row_map).cuda(), torch.from_numpy(mult).cuda()))
+    xf = x.float().numpy().astype(np.float64)
+    vals = (mult.astype(np.float64)[:, None] * xf[row_map]).astype(np.float32)
+    want_q, want_s = quant_128x1_grouped(vals, offs, rule)
+    _check_q1(B, offs, qT, sT, want_q, want_s)
+
+
+@gpu
+def test_transpose_fp8_blocks():
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding as B
+    rng = np.random.default_rng(13)
+    b, rows, cols = 3, 256, 384
+    q = _codes(rng, (b, rows, cols))
+    s = rng.uniform(0.1, 2, (b, rows // 128, cols // 128)).astype(np.float32)
+    qT, sT = B.transpose_fp8_blocks(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda())
+    assert np.array_equal(to_np(qT), q.transpose(0, 2, 1))
+    assert np.array_equal(to_np(sT), s.transpose(0, 2, 1))
+    # two matrices side by side, padded rows left alone
+    wide = torch.full((b, cols + 128, 2 * rows), 7, dtype=torch.uint8, device="cuda")
+    wide_s = torch.full((b, (cols + 128) // 128, 2 * rows // 128), -1.0, device="cuda")
+    B.transpose_fp8_blocks(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), wide, wide_s, offset=rows)
+    w = to_np(wide)
+    assert np.array_equal(w[:, :cols, rows:], q.transpose(0, 2, 1))
+    assert (w[:, :cols, :rows] == 7).all() and (w[:, cols:] == 7).all()
+    assert np.array_equal(to_np(wide_s)[:, :cols // 128, rows // 128:], s.transpose(0, 2, 1))
+
+
+@gpu
+@pytest.mark.parametrize("sizes", [SIZES, [0, 0, 1], [1024, 64, 0, 640]])
+def test_grouped_wgrad_fp8(sizes):
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding as B
+    rng = np.random.default_rng(14)
+    offs = _offsets(sizes)
+    G = len(sizes)
+    P = segment_starts(offs)
+    M, N = 256, 512
+    width = B.q1_width(G, int(offs[-1]))
+    aT = np.zeros((M, width), np.uint8)
+    bT = np.zeros((N, width), np.uint8)
+    aT[:, :P[-1]] = _codes(rng, (M, int(P[-1])))
+    bT[:, :P[-1]] = _codes(rng, (N, int(P[-1])))
+    saT = rng.uniform(1e-3, 1e-2, (width // 128, M)).astype(np.float32)
+    sbT = rng.uniform(1e-3, 1e-2, (width // 128, N)).astype(np.float32)
+    out = B.grouped_wgrad_fp8(torch.from_numpy(offs).cuda(), int(offs[-1]), torch.from_numpy(aT).cuda(),
+                              torch.from_numpy(saT).cuda(), torch.from_numpy(bT).cuda(), torch.from_numpy(sbT).cuda())
+    B.check_device_status()
+    got = to_np(out)
+    for g in range(G):
+        c0, c1 = int(P[g]), int(P[g + 1])
+        if c1 == c0:
+            assert not got[g].any(), f"group {g} has no rows but a nonzero gradient"
+            continue
+        want = gemm_fp8_wgrad(aT[:, c0:c1], saT[c0 // 128:c1 // 128], bT[:, c0:c1], sbT[c0 // 128:c1 // 128])
+        rel = np.linalg.norm(got[g] - want) / np.linalg.norm(want)
+        assert rel < 1e-5, f"group {g}: rel-L2 {rel:.3e}"
+
+
+@gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
+def test_swiglu_backward(rule):
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding as B
+    rng = np.random.default_rng(15)
+    rows, I = 200, 384
+    a = (rng.standard_normal((rows, I)) * 3).astype(np.float32)
+    b = (rng.standard_normal((rows, I)) * 2).astype(np.float32)
+    dh = rng.standard_normal((rows, I + 128)).astype(np.float32)
+    # gate/up tile layout: I-block j -> gate[128j..+64) up[..] gate[128j+64..+128) up[..]
+    ab = np.empty((rows, 2 * I), np.float32)
+    for j in range(I // 128):
+        for h in range(2):
+            sl = slice(128 * j + 64 * h, 128 * j + 64 * h + 64)
+            ab[:, 256 * j + 128 * h: 256 * j + 128 * h + 64] = a[:, sl]
+            ab[:, 256 * j + 128 * h + 64: 256 * j + 128 * h + 128] = b[:, sl]
+    abt = torch.from_numpy(ab).cuda()
+    q = torch.empty(rows, 2 * I, dtype=torch.uint8, device="cuda")
+    s = torch.empty(rows, 2 * I // 128, dtype=torch.float32, device="cuda")
+    B.swiglu_backward(abt, torch.from_numpy(dh).cuda(), q, s, rule)
+    dA, dB = swiglu_grad(a, b, dh[:, :I])
+    out = to_np(abt)
+    got_a = np.empty_like(a)
+    got_b = np.empty_like(b)
+    for j in range(I // 128):
+        for h in range(2):
+            sl = slice(128 * j + 64 * h, 128 * j + 64 * h + 64)
+            got_a[:, sl] = out[:, 256 * j + 128 * h: 256 * j + 128 * h + 64]
+            got_b[:, sl] = out[:, 256 * j + 128 * h + 64: 256 * j + 128 * h + 128]
+    for got, want in ((got_a, dA), (got_b, dB)):
+        err = np.abs(got - want) / (np.abs(want).max(axis=1, keepdims=True) + 1e-30)
+        assert err.max() < 1e-5
+    # 1x128 E4M3 of [dA | dB]: the oracle quantises its own float32 rounding of the exact values,
+    # so an element whose two roundings straddle an E4M3 rounding boundary may differ by one code
+    wq, ws = quant_1x128(np.concatenate([dA, dB], axis=1).astype(np.float32), rule)
+    gq, gs = to_np(q), to_np(s)
+    np.testing.assert_allclose(gs, ws, rtol=1e-5)
+    same = gq == wq
+    assert same.mean() > 0.999
+    dq = e4m3.decode(gq[~same]).astype(np.float64)
+    dw = e4m3.decode(wq[~same]).astype(np.float64)
+    assert (np.abs(dq - dw) <= np.abs(dw) * 0.125 + 2.0 ** -9).all()
+
+
+@gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
+def test_combine_backward(rule):
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding
+    from sparse_moe_layer_13_b300.configs import MoEConfig
+    cfg = MoEConfig("t", T=96, d=384, E=16, I=128, K=4, G=4, M=2, gk=2, seed=0)
+    rng = np.random.default_rng(16)
+    T, K, d = cfg.T, cfg.K, cfg.d
+    dy = _bf16(rng.standard_normal((T, d)))
+    routed = _bf16(rng.standard_normal((T * K, d)))
+    row_of = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+    gate = rng.uniform(0.01, 0.7, (T, K)).astype(np.float32)
+    dev = lambda a: torch.from_numpy(a).cuda()  # noqa: E731
+    dOq = torch.empty(cfg.rows, d, dtype=torch.uint8, device="cuda")
+    dOs = torch.empty(cfg.rows, d // 128, dtype=torch.float32, device="cuda")
+    rgate = torch.empty(cfg.rows, dtype=torch.float32, device="cuda")
+    dgate = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    binding.combine_backward(cfg, dy.cuda(), routed.cuda(), dev(row_of), dev(gate), dOq, dOs, rgate, dgate, rule)
+    binding.check_device_status()
+    dyf = dy.float().numpy().astype(np.float64)
+    rf = routed.float().numpy().astype(np.float64)
+    vals = np.zeros((cfg.rows, d), np.float32)
+    want_rg = np.ones(cfg.rows, np.float32)
+    for t in range(T):
+        for k in range(K):
+            vals[row_of[t, k]] = (np.float64(gate[t, k]) * dyf[t]).astype(np.float32)
+            want_rg[row_of[t, k]] = gate[t, k]
+        vals[T * K + t] = dyf[t]
+    wq, ws = quant_1x128(vals, rule)
+    assert np.array_equal(to_np(dOq), wq)
+    assert np.array_equal(to_np(dOs).view(np.uint32), ws.view(np.uint32))
+    assert np.array_equal(to_np(rgate), want_rg)
+    want_dg = np.array([[dyf[t] @ rf[row_of[t, k]] for k in range(K)] for t in range(T)])
+    np.testing.assert_allclose(to_np(dgate), want_dg, rtol=1e-4, atol=1e-4 * np.abs(want_dg).max())
+
+
+# ----------------------------------------------------------------- the layer ----
+def _unpack_w13(dW13_e, I):
+    """Rows of a gradient in the SwiGLU tile layout -> (dW1 [I][*], dW3 [I][*])."""
+    p = np.arange(2 * I)
+    j, q = p // 256, p % 256
+    up = ((q >= 64) & (q < 128)) | (q >= 192)
+    i = 128 * j + np.where(q < 128, q % 64, 64 + q % 64)
+    dW1 = np.empty((I, dW13_e.shape[1]), dW13_e.dtype)
+    dW3 = np.empty_like(dW1)
+    dW1[i[~up]] = dW13_e[~up]
+    dW3[i[up]] = dW13_e[up]
+    return dW1, dW3
+
+
+def _backward_case(cfg, tokens=None, wgrad_experts=None, router_experts=None, rule="fp32", seed=0):
+    from sparse_moe_layer_13_b300 import binding, inputs
+    from sparse_moe_layer_13_b300.layer import MoELayer
+    layer = MoELayer(cfg, "cuda", scale_rule=rule, backward=True)
+    x = inputs.gen_x(cfg, "cuda")
+    dy = inputs.gen_dy(cfg, "cuda")
+    b0 = to_np(layer.bias).copy()
+    layer.forward(x, update_bias=False)
+    g = layer.backward(x, dy)
+    binding.check_device_status()
+    xn, Wr, dyn = to_np(x), to_np(layer.Wr), to_np(dy)
+    ref_idx, ref_gate, info = oracle_route(xn, Wr, b0, cfg.G, cfg.M, cfg.K, cfg.gk)
+    assert np.array_equal(to_np(layer.idx)[~near_tie(info)], ref_idx[~near_tie(info)])
+    tie = near_tie(info)
+    assert not tie.any(), "a near-tie token changes the gradient's support; pick another seed"
+    s_sel = np.take_along_axis(affinity(xn, Wr), ref_idx, axis=1)
+    rng = np.random.default_rng(seed)
+    tokens = np.arange(cfg.T) if tokens is None else np.sort(rng.choice(cfg.T, tokens, replace=False))
+    if wgrad_experts is None:
+        wgrad_experts = list(range(cfg.E + 1))
+    if router_experts is None:
+        router_experts = list(range(cfg.E))
+    need = set(ref_idx[tokens].ravel().tolist()) | {cfg.E} | set(wgrad_experts)
+    for e in router_experts:
+        for t in np.nonzero((ref_idx == e).any(axis=1))[0]:
+            need |= set(ref_idx[t].tolist())
+    ex = oracle_experts(cfg, need, rule=rule)
+    deq = {e: dequant_expert(w) for e, w in ex.items()}
+    Q = Quantiser(rule)
+    ref = layer_backward(cfg, xn, dyn, Wr, ref_idx, s_sel, lambda e: deq[e], tokens=tokens,
+                         wgrad_experts=wgrad_experts, router_experts=router_experts, Q=Q)
+    print(f"[backward {cfg.name} {rule}] dx over {len(tokens)} tokens")
+    assert_y_close(to_np(g["dx"])[tokens], ref["dx"])
+    assert_y_close(to_np(g["dz"])[tokens], ref["dz"])
+    assert_y_close(to_np(g["dgate"])[tokens], ref["dg"])
+    for e in wgrad_experts:
+        dW1, dW3, dW2 = ref["dW"][e]
+        g1, g3 = _unpack_w13(to_np(g["dW13"][e]), cfg.I)
+        print(f"[backward {cfg.name} {rule}] expert {e} weight gradients")
+        assert_y_close(g1, dW1)
+        assert_y_close(g3, dW3)
+        assert_y_close(to_np(g["dW2T"][e]).T, dW2)
+    if router_experts:
+        print(f"[backward {cfg.name} {rule}] router rows {len(router_experts)}")
+        got = to_np(g["dWr"])[router_experts]
+        want = np.stack([ref["dWr"][e] for e in router_experts])
+        assert_y_close(got, want)
+    return layer
+
+
+@gpu
+@pytest.mark.parametrize("rule", ["fp32", "pow2"])
+def test_layer_backward_tiny(rule):
+    require_gpu()
+    _backward_case(CONFIGS["tiny"], rule=rule)
+
+
+@gpu
+def test_layer_backward_mid_sampled():
+    require_gpu()
+    _backward_case(CONFIGS["mid"], tokens=48, wgrad_experts=[0, 37, 64], router_experts=[5, 63])
+
+
+@gpu
+def test_layer_backward_full_sampled():
+    require_gpu()
+    _backward_case(CONFIGS["full"], tokens=12, wgrad_experts=[3, 200], router_experts=[])
