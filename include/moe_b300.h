@@ -375,10 +375,14 @@ moe_status moe_transpose_fp8_blocks(const uint8_t* q, const float* scale, int64_
 
 /* Backward of moe_combine for upstream gradient dy (bf16 [T][d]):
  *   dgate[t][k] = sum_n dy[t][n] * routed_out[row_of[t][k]][n]   (FP32)
- *   the expert-output gradient of each grouped row, quantised per 1x128 tile
- *   with scale rule `rule`: row row_of[t][k] holds fl32(topk_gate[t][k] * dy[t]),
- *   shared row T*K + t holds dy[t]; codes dOq u8 [T*K+T][d], scales dOs
- *   f32 [T*K+T][d/128];
+ *   the expert-output gradient of each grouped row, quantised per 1x128 tile:
+ *   row row_of[t][k] holds g * dy[t] (g = topk_gate[t][k] > 0), shared row
+ *   T*K + t holds dy[t]; codes dOq u8 [T*K+T][d], scales dOs f32 [T*K+T][d/128].
+ *   MOE_SCALE_FP32: every row of token t takes the codes of dy[t]'s own tile
+ *   and scale fl32(g * s) with s = fl32(amax/448) of that tile (the 1x128
+ *   quantisation of g * dy, g scaling the tile uniformly);
+ *   MOE_SCALE_POW2: fl32(g * dy[t]) quantised row by row (a power-of-two
+ *   scale cannot absorb g);
  *   row_gate f32 [T*K+T]: the gate of each grouped row (1 for shared rows).
  * routed_out bf16 [T*K][d] (the forward's routed expert outputs); row_of,
  * topk_gate as in moe_combine. */

@@ -6,7 +6,7 @@
 // held fixed; gradients flow through the gates, the sigmoid affinities and
 // the SwiGLU experts.
 //
-//   combine_backward_kernel   dg = dy . out_k, dO_k = fl32(g_k dy) -> 1x128 E4M3
+//   combine_backward_kernel   dg = dy . out_k, dO_k = g_k dy -> 1x128 E4M3
 //   route_backward_kernel     dz_k = ds_k s_k (1 - s_k), ds = (dg - g.dg) / S
 //   router_wgrad_kernel       dWr[e] = sum over e's rows of dz * x
 //   swiglu_backward_kernel    dA, dB of h = SiLU(a) b; 1x128 E4M3 of [dA | dB]
@@ -46,6 +46,13 @@ __device__ __forceinline__ float warp_sum(float v) {
 // tiles w, w+8, ...; lane l holds 4 columns. rgate[r] receives the gate of
 // grouped row r (1 for shared rows). dgate sums the per-warp partial dot
 // products in warp order.
+// The expert-output gradient of routed row k is g_k * dy[t]. Since g_k > 0
+// scales a tile uniformly, its 1x128 quantisation under the FP32 rule has
+// the codes of dy's own tile and the scale g_k * s_dy: the tile is quantised
+// once and every row gets scale fl32(g_k * s_dy). (Quantising fl32(g_k * dy)
+// again would put the ratios 448 * y / y_max, often exact E4M3 midpoints for
+// bf16 dy, at the mercy of the gate's last bit.) A power-of-two scale cannot
+// absorb g_k, so POW2 quantises fl32(g_k * dy) row by row.
 template <bool POW2>
 __global__ void __launch_bounds__(256)
 combine_backward_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restrict__ routed,
@@ -74,36 +81,55 @@ combine_backward_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restr
     const int lane = static_cast<int>(lane_id());
     const int ntile = d / 128;
     const uint16_t* dyt = dy + static_cast<int64_t>(t) * d;
-    for (int k = 0; k <= K; ++k) {
-        const int64_t r = rows[k];
-        const float g = gates[k];
-        float part = 0.0f;
-        for (int tile = warp; tile < ntile; tile += 8) {
-            const int64_t col = static_cast<int64_t>(tile) * 128 + lane * 4;
-            const uint2 u = __ldg(reinterpret_cast<const uint2*>(dyt + col));
-            const float y0 = bf16_lo(u.x), y1 = bf16_hi(u.x), y2 = bf16_lo(u.y), y3 = bf16_hi(u.y);
-            float v0 = y0, v1 = y1, v2 = y2, v3 = y3;
-            if (k < K) {
-                if (r >= 0) {
-                    const uint2 o = __ldg(reinterpret_cast<const uint2*>(routed + r * d + col));
-                    part = fmaf(y0, bf16_lo(o.x), part);
-                    part = fmaf(y1, bf16_hi(o.x), part);
-                    part = fmaf(y2, bf16_lo(o.y), part);
-                    part = fmaf(y3, bf16_hi(o.y), part);
-                }
-                v0 = __fmul_rn(g, y0); v1 = __fmul_rn(g, y1); v2 = __fmul_rn(g, y2); v3 = __fmul_rn(g, y3);
+    float part[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) part[k] = 0.0f;
+    for (int tile = warp; tile < ntile; tile += 8) {
+        const int64_t col = static_cast<int64_t>(tile) * 128 + lane * 4;
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(dyt + col));
+        const float y0 = bf16_lo(u.x), y1 = bf16_hi(u.x), y2 = bf16_lo(u.y), y3 = bf16_hi(u.y);
+        // dg partial sums (K <= 16, unrolled so part[] stays in registers)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (k < K && rows[k] >= 0) {
+                const uint2 o = __ldg(reinterpret_cast<const uint2*>(routed + rows[k] * d + col));
+                part[k] = fmaf(y0, bf16_lo(o.x), part[k]);
+                part[k] = fmaf(y1, bf16_hi(o.x), part[k]);
+                part[k] = fmaf(y2, bf16_lo(o.y), part[k]);
+                part[k] = fmaf(y3, bf16_hi(o.y), part[k]);
             }
-            const float amax = warp_max(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
-            const float s = tile_scale<POW2>(amax);
-            if (r >= 0) {
+        }
+        if (!POW2) {
+            const float amax = warp_max(fmaxf(fmaxf(fabsf(y0), fabsf(y1)), fmaxf(fabsf(y2), fabsf(y3))));
+            const float s = tile_scale<false>(amax);
+            const uint32_t codes =
+                e4m3x4(quant_ratio(y0, s), quant_ratio(y1, s), quant_ratio(y2, s), quant_ratio(y3, s));
+            for (int k = 0; k <= K; ++k) {
+                const int64_t r = rows[k];
+                if (r < 0) continue;
+                *reinterpret_cast<uint32_t*>(dOq + r * d + col) = codes;
+                if (lane == 0) dOs[r * ntile + tile] = k < K ? __fmul_rn(gates[k], s) : s;
+            }
+        } else {
+            for (int k = 0; k <= K; ++k) {
+                const int64_t r = rows[k];
+                const float g = gates[k];
+                float v0 = y0, v1 = y1, v2 = y2, v3 = y3;
+                if (k < K) { v0 = __fmul_rn(g, y0); v1 = __fmul_rn(g, y1); v2 = __fmul_rn(g, y2); v3 = __fmul_rn(g, y3); }
+                const float amax = warp_max(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
+                const float s = tile_scale<true>(amax);
+                if (r < 0) continue;
                 *reinterpret_cast<uint32_t*>(dOq + r * d + col) =
                     e4m3x4(quant_ratio(v0, s), quant_ratio(v1, s), quant_ratio(v2, s), quant_ratio(v3, s));
                 if (lane == 0) dOs[r * ntile + tile] = s;
             }
         }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
         if (k < K) {
-            part = warp_sum(part);
-            if (lane == 0) red[warp][k] = part;
+            const float p = warp_sum(part[k]);
+            if (lane == 0) red[warp][k] = p;
         }
     }
     __syncthreads();

@@ -5,24 +5,45 @@ scales and transposed bytes; FP32 tolerances for sums), then the whole
 layer backward on the workload shapes: every gradient at tiny size, sampled
 tokens and experts at mid and full width.
 
-Tolerances for the layer gradients are the layer output's (relative L2
-<= 5e-3, max |diff| <= 2e-2 * RMS): the backward GEMMs quantise to E4M3 at
-the same kind of points as the forward, and each gradient is one more chain
-of FP8 GEMMs with FP32 promotion.
+Tolerances for the layer gradients, derived from where the two sides may
+differ. The gradient GEMMs requantise their FP32 inputs (dO, dA, dB) to
+E4M3, and those inputs differ between the two sides by the accumulation
+error of the GEMMs that made them (up to ~1e-5 relative: tensor-core chunk
+sums before their FP32 promotion). An element within that distance of an
+E4M3 rounding midpoint may take the neighbouring code, moving it by one
+step: up to 1/14 of its tile's largest value. Through a weight of
+magnitude up to ~4/sqrt(d) that is up to ~3-6% of the gradient's RMS in one
+element at the tiny width (d = 256), less at larger widths. Expected flips
+grow with the width about as fast as each one's effect shrinks, giving
+~5e-3 relative L2 at every width, plus ~2e-3 from the bf16 storage of the
+routed rows and of dx. Hence, over every element: relative L2 <= 1e-2,
+max |diff| <= 1e-1 * RMS. On the tokens (rows) the oracle does not flag
+(no quantised gradient element of theirs within 3e-5 of a midpoint) the
+forward's bounds hold: relative L2 <= 5e-3, max |diff| <= 2e-2 * RMS.
+Weight gradients sum few rows per expert (64 at the tiny size), so one
+flipped step of a 128x1 tile moves a whole gradient row by a few per cent:
+over every element relative L2 <= 3e-2, max |diff| <= 3e-1 * RMS; the
+forward's bounds on the rows (and W2 columns) with no flagged operand
+channel.
 """
 import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_y_close, gpu, oracle_experts, require_gpu, to_np
+from gpu_helpers import assert_y_close, check_routing, gpu, oracle_experts, require_gpu, to_np, y_metrics
 from oracle import e4m3
 from oracle.backward import (Quantiser, dequant_expert, gemm_fp8_wgrad, layer_backward, quant_128x1_grouped,
                              segment_starts, swiglu_grad)
 from oracle.quant import quant_1x128
-from oracle.route import affinity, near_tie, route as oracle_route
+from oracle.route import affinity, route as oracle_route
 from sparse_moe_layer_13_b300.configs import CONFIGS
 
 SIZES = [0, 5, 130, 128, 1, 0, 257, 384]
+# bounds over every element, flagged ones included (see the module docstring)
+GRAD_REL_L2 = 1e-2
+GRAD_MAX_RMS = 1e-1
+WGRAD_REL_L2 = 3e-2
+WGRAD_MAX_RMS = 3e-1
 
 
 def _offsets(sizes):
@@ -217,14 +238,21 @@ def test_combine_backward(rule):
     binding.check_device_status()
     dyf = dy.float().numpy().astype(np.float64)
     rf = routed.float().numpy().astype(np.float64)
-    vals = np.zeros((cfg.rows, d), np.float32)
     want_rg = np.ones(cfg.rows, np.float32)
+    rows_g = np.ones(cfg.rows)
+    src = np.zeros((cfg.rows, d), np.float32)
     for t in range(T):
         for k in range(K):
-            vals[row_of[t, k]] = (np.float64(gate[t, k]) * dyf[t]).astype(np.float32)
+            src[row_of[t, k]] = dyf[t]
+            rows_g[row_of[t, k]] = gate[t, k]
             want_rg[row_of[t, k]] = gate[t, k]
-        vals[T * K + t] = dyf[t]
-    wq, ws = quant_1x128(vals, rule)
+        src[T * K + t] = dyf[t]
+    if rule == "fp32":
+        # codes of dy's own tiles, scale fl32(g * s)
+        wq, s_dy = quant_1x128(src, rule)
+        ws = (rows_g[:, None] * s_dy.astype(np.float64)).astype(np.float32)
+    else:
+        wq, ws = quant_1x128((rows_g[:, None] * src.astype(np.float64)).astype(np.float32), rule)
     assert np.array_equal(to_np(dOq), wq)
     assert np.array_equal(to_np(dOs).view(np.uint32), ws.view(np.uint32))
     assert np.array_equal(to_np(rgate), want_rg)
@@ -246,6 +274,24 @@ def _unpack_w13(dW13_e, I):
     return dW1, dW3
 
 
+def _check_grad(name, got, want, rows=None, cols=None, rel_all=GRAD_REL_L2, max_all=GRAD_MAX_RMS):
+    """Bounds over every element, then the forward's bounds on the unflagged rows/columns."""
+    rel, mx = y_metrics(got, want)
+    print(f"[parity] {name}: rel-L2 {rel:.3e} max-abs/RMS {mx:.3e} over every element")
+    assert rel <= rel_all, f"{name}: rel-L2 {rel:.3e}"
+    assert mx <= max_all, f"{name}: max-abs/RMS {mx:.3e}"
+    keep_r = np.ones(got.shape[0], bool) if rows is None else ~rows
+    keep_c = np.ones(got.shape[1], bool) if cols is None else ~cols
+    if keep_r.any() and keep_c.any():
+        assert_y_close(got[keep_r][:, keep_c], want[keep_r][:, keep_c])
+
+
+def _by_expert(v, idx):
+    """Per-token values of the K slots, reordered by expert index (the slot order of near-equal
+    biased affinities may differ between the two sides)."""
+    return np.take_along_axis(v, np.argsort(idx, axis=1), axis=1)
+
+
 def _backward_case(cfg, tokens=None, wgrad_experts=None, router_experts=None, rule="fp32", seed=0):
     from sparse_moe_layer_13_b300 import binding, inputs
     from sparse_moe_layer_13_b300.layer import MoELayer
@@ -258,16 +304,16 @@ def _backward_case(cfg, tokens=None, wgrad_experts=None, router_experts=None, ru
     binding.check_device_status()
     xn, Wr, dyn = to_np(x), to_np(layer.Wr), to_np(dy)
     ref_idx, ref_gate, info = oracle_route(xn, Wr, b0, cfg.G, cfg.M, cfg.K, cfg.gk)
-    assert np.array_equal(to_np(layer.idx)[~near_tie(info)], ref_idx[~near_tie(info)])
-    tie = near_tie(info)
-    assert not tie.any(), "a near-tie token changes the gradient's support; pick another seed"
+    gidx = to_np(layer.idx)
+    tie, _ = check_routing(cfg, gidx, to_np(layer.gate), ref_idx, ref_gate, info)
     s_sel = np.take_along_axis(affinity(xn, Wr), ref_idx, axis=1)
     rng = np.random.default_rng(seed)
-    tokens = np.arange(cfg.T) if tokens is None else np.sort(rng.choice(cfg.T, tokens, replace=False))
-    if wgrad_experts is None:
-        wgrad_experts = list(range(cfg.E + 1))
-    if router_experts is None:
-        router_experts = list(range(cfg.E))
+    ok_tok = np.nonzero(~tie)[0]
+    tokens = ok_tok if tokens is None else np.sort(rng.choice(ok_tok, tokens, replace=False))
+    # an expert's weight gradient sums over its rows: only experts no near-tie token reaches
+    tied = set(ref_idx[tie].ravel().tolist()) | set(gidx[tie].ravel().tolist())
+    wgrad_experts = [e for e in (range(cfg.E + 1) if wgrad_experts is None else wgrad_experts) if e not in tied]
+    router_experts = [e for e in (range(cfg.E) if router_experts is None else router_experts) if e not in tied]
     need = set(ref_idx[tokens].ravel().tolist()) | {cfg.E} | set(wgrad_experts)
     for e in router_experts:
         for t in np.nonzero((ref_idx == e).any(axis=1))[0]:
@@ -277,22 +323,27 @@ def _backward_case(cfg, tokens=None, wgrad_experts=None, router_experts=None, ru
     Q = Quantiser(rule)
     ref = layer_backward(cfg, xn, dyn, Wr, ref_idx, s_sel, lambda e: deq[e], tokens=tokens,
                          wgrad_experts=wgrad_experts, router_experts=router_experts, Q=Q)
-    print(f"[backward {cfg.name} {rule}] dx over {len(tokens)} tokens")
-    assert_y_close(to_np(g["dx"])[tokens], ref["dx"])
-    assert_y_close(to_np(g["dz"])[tokens], ref["dz"])
-    assert_y_close(to_np(g["dgate"])[tokens], ref["dg"])
+    near = ref["near"]
+    print(f"[backward {cfg.name} {rule}] {len(tokens)} tokens, {near.sum()} flagged (a quantised gradient "
+          f"element within {Q.tol:g} of an E4M3 rounding midpoint)")
+    _check_grad("dx", to_np(g["dx"])[tokens], ref["dx"], rows=near)
+    ti = ref_idx[tokens]
+    _check_grad("dz", _by_expert(to_np(g["dz"])[tokens], gidx[tokens]), _by_expert(ref["dz"], ti), rows=near)
+    _check_grad("dgate", _by_expert(to_np(g["dgate"])[tokens], gidx[tokens]), _by_expert(ref["dg"], ti), rows=near)
     for e in wgrad_experts:
-        dW1, dW3, dW2 = ref["dW"][e]
+        dW1, dW3, dW2, fl = ref["dW"][e]
         g1, g3 = _unpack_w13(to_np(g["dW13"][e]), cfg.I)
-        print(f"[backward {cfg.name} {rule}] expert {e} weight gradients")
-        assert_y_close(g1, dW1)
-        assert_y_close(g3, dW3)
-        assert_y_close(to_np(g["dW2T"][e]).T, dW2)
+        g2 = to_np(g["dW2T"][e]).T
+        r2, c2 = fl["dW2"]
+        print(f"[backward {cfg.name} {rule}] expert {e}: flagged rows dW1 {fl['dW1'].sum()} dW3 {fl['dW3'].sum()} "
+              f"dW2 {r2.sum()} (columns {c2.sum()})")
+        _check_grad(f"dW1[{e}]", g1, dW1, rows=fl["dW1"], rel_all=WGRAD_REL_L2, max_all=WGRAD_MAX_RMS)
+        _check_grad(f"dW3[{e}]", g3, dW3, rows=fl["dW3"], rel_all=WGRAD_REL_L2, max_all=WGRAD_MAX_RMS)
+        _check_grad(f"dW2[{e}]", g2, dW2, rows=r2, cols=c2, rel_all=WGRAD_REL_L2, max_all=WGRAD_MAX_RMS)
     if router_experts:
-        print(f"[backward {cfg.name} {rule}] router rows {len(router_experts)}")
         got = to_np(g["dWr"])[router_experts]
         want = np.stack([ref["dWr"][e] for e in router_experts])
-        assert_y_close(got, want)
+        _check_grad("dWr", got, want)
     return layer
 
 

@@ -16,7 +16,7 @@ import pytest
 
 from oracle import e4m3
 from oracle.backward import (Quantiser, dequant_128x1_grouped, gate_grad, gemm_fp8_wgrad, layer_backward,
-                             quant_128x1_grouped, segment_starts, swiglu_grad)
+                             near_midpoint, quant_128x1_grouped, segment_starts, swiglu_grad)
 
 
 class _Cfg:
@@ -81,6 +81,7 @@ def test_exact_gradients_match_finite_differences():
     for e in range(cfg.E + 1):
         for j, name in enumerate(("W1", "W3", "W2")):
             np.testing.assert_allclose(r["dW"][e][j], _fd(f, W[e][j]), rtol=1e-6, atol=1e-7, err_msg=f"{name}[{e}]")
+        assert not r["dW"][e][3]["dW1"].any()              # nothing is flagged without quantisation
 
 
 def test_swiglu_grad_finite_differences():
@@ -186,3 +187,37 @@ def test_quantised_gradients_near_exact():
     for e in range(E + 1):
         for j in range(3):
             assert rel(quant["dW"][e][j], exact["dW"][e][j]) < 0.08
+
+
+def test_near_midpoint():
+    # E4M3 grid around 1: spacing 1/8 in [1, 2), 1/16 in [0.5, 1); 448 is the top value
+    assert near_midpoint(np.array([1.0625]))[0]                     # the midpoint of 1 and 1.125
+    assert near_midpoint(np.array([1.0625 * (1 + 1e-5)]))[0]
+    assert not near_midpoint(np.array([1.0625 * (1 + 1e-4)]))[0]
+    assert not near_midpoint(np.array([1.0, 1.125, 0.0, 448.0, 40.0])).any()
+    assert near_midpoint(np.array([0.53125]))[0]                    # midpoint of 0.5 and 0.5625
+    assert near_midpoint(np.array([2.0 ** -10]))[0]                 # subnormal grid, spacing 2^-9
+    # a value on a midpoint is exactly where encode's tie rule decides: flipping the
+    # last FP32 bit either way moves the code by one
+    for v in (1.0625, 0.53125, 42.0, -304.0):
+        up = e4m3.encode(np.nextafter(np.float32(v), np.float32(np.inf)))
+        dn = e4m3.encode(np.nextafter(np.float32(v), np.float32(-np.inf)))
+        assert up != dn and near_midpoint(np.array([v]))[0]
+
+
+def test_scaled_rows_reduces_to_plain_quantisation():
+    """g * y with g = 1 or a power of two is quantised exactly like the plain 1x128 rule."""
+    from oracle.quant import dequant_1x128, quant_1x128
+    rng = np.random.default_rng(6)
+    y = rng.standard_normal((9, 256)).astype(np.float32)
+    for rule in ("fp32", "pow2"):
+        Q = Quantiser(rule)
+        for g in (1.0, 0.25, 2.0 ** -7):
+            got = Q.scaled_rows(y, np.full(9, g))
+            want = dequant_1x128(*quant_1x128((g * y).astype(np.float32), rule))
+            assert np.array_equal(got, want), (rule, g)
+    # a general gate: within one E4M3 step of g * y, the scale g times the plain scale
+    g = rng.uniform(0.05, 0.9, 9)
+    got = Quantiser("fp32").scaled_rows(y, g)
+    q, s = quant_1x128(y, "fp32")
+    np.testing.assert_allclose(got, dequant_1x128(q, s) * g[:, None], rtol=2 ** -23)
