@@ -9,6 +9,7 @@ update.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config full]
   python bench.py --impl reference ...   # the FP64 CPU oracle on a token sample
+  python bench.py --backward ...         # a training step: forward, bias update, backward
 
 Under torchrun (N > 1) each rank runs its own layer on its own tokens (weak
 scaling); the only exchange is an all-reduce of the per-expert load before
@@ -258,6 +259,126 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+TRAIN_METRIC = "MoE layer forward+backward tokens/s; FP8 weight-gradient GEMM TFLOP/s & % of roofline (1 B300)"
+
+
+def run_train(args):
+    """--backward: a training step of the layer (forward, bias update, backward) on one GPU."""
+    import torch
+
+    import __graft_entry__
+    from sparse_moe_layer_13_b300 import binding, inputs
+    from sparse_moe_layer_13_b300.configs import CONFIGS, PROFILE_CONFIGS
+    from sparse_moe_layer_13_b300.layer import MoELayer
+
+    torch.cuda.set_device(0)
+    __graft_entry__.build()
+    cfg = {**CONFIGS, **PROFILE_CONFIGS}[args.config]
+    layer = MoELayer(cfg, "cuda", scale_rule=args.scales, backward=True)
+    x = inputs.gen_x(cfg, "cuda")
+    dy = inputs.gen_dy(cfg, "cuda")
+    names = ("gemm1", "gemm2")
+    bnames = ("dgrad2", "recompute", "dgrad1", "wgrad2", "wgrad1")
+    K = args.steps
+
+    def _step(i=None, ev=None):
+        layer.forward(x, update_bias=False, events=None if ev is None else {n: ev[n][i] for n in names})
+        binding.bias_update(cfg.E, cfg.T, cfg.K, layer.counts, cfg.gamma, layer.bias)
+        return layer.backward(x, dy, events=None if ev is None else {n: ev[n][i] for n in bnames})
+
+    for _ in range(args.warmup):
+        _step()
+    torch.cuda.synchronize()
+    binding.check_device_status()
+    ev = {n: [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+              for _ in range(K)] for n in names + bnames}
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(K):
+                _step(i, ev)
+        graph.replay()
+        torch.cuda.synchronize()
+        binding.check_device_status()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clocks:
+        torch.cuda.synchronize()
+        t0.record()
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(K):
+                _step(i, ev)
+        t1.record()
+        torch.cuda.synchronize()
+    binding.check_device_status()
+    ms = t0.elapsed_time(t1) / K
+    kt = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names + bnames}
+
+    # end to end: x and dy from pinned host memory, dx back, every step (serial copies)
+    xh, dyh = x.cpu().pin_memory(), dy.cpu().pin_memory()
+    dxh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K):
+        xd.copy_(xh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        layer.forward(xd, update_bias=False)
+        binding.bias_update(cfg.E, cfg.T, cfg.K, layer.counts, cfg.gamma, layer.bias)
+        dxh.copy_(layer.backward(xd, dyd)["dx"], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+
+    hbm, bf16, _, src = _peaks()
+    fp8_peak = 2.0 * bf16
+    R, d, I, E1 = cfg.rows, cfg.d, cfg.I, cfg.E + 1
+    # weight gradient of W1|W3: 2 * rows * 2I * d FLOPs; its bytes: the FP32 gradient written
+    # (E+1) * 2I * d * 4, plus both transposed E4M3 operands and their 128x1 scales read once
+    width = binding.q1_width(E1, R)
+    w1_flops = 2.0 * R * 2 * I * d
+    w1_bytes = E1 * 2 * I * d * 4 + (2 * I + d) * width * (1 + 4 / 128)
+    w1_ms = kt["wgrad1"]
+    t_tensor, t_hbm = w1_flops / (fp8_peak * 1e12), w1_bytes / (hbm * 1e9)
+    if t_hbm > t_tensor:
+        roof = {"kernel": "grouped_wgrad_fp8 (dW1|dW3)", "bound": "hbm",
+                "achieved": round(w1_bytes / (w1_ms * 1e-3) / 1e9, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(w1_bytes / (w1_ms * 1e-3) / 1e9 / hbm, 4), "traffic": None,
+                "algorithmic_bytes": round(w1_bytes), "peak_source": f"{src}: HBM copy bandwidth"}
+    else:
+        roof = {"kernel": "grouped_wgrad_fp8 (dW1|dW3)", "bound": "tensor",
+                "achieved": round(w1_flops / (w1_ms * 1e-3) / 1e12, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(w1_flops / (w1_ms * 1e-3) / 1e12 / fp8_peak, 4), "traffic": None,
+                "peak_source": f"{src}: bf16 burst {bf16} TFLOP/s x 2 (E4M3/bf16 nominal ratio)"}
+    roof["tensor_frac"] = round(w1_flops / (w1_ms * 1e-3) / 1e12 / fp8_peak, 4)
+    roof["hbm_frac"] = round(w1_bytes / (w1_ms * 1e-3) / 1e9 / hbm, 4)
+    f1, f2 = cfg.gemm_flops()
+    # algorithmic backward FLOPs: data and weight gradients of both GEMMs (the recomputation of
+    # the gate/up pre-activations, another f1, is work done but not counted)
+    bwd_flops = 2 * f1 + 2 * f2
+    out = {
+        "metric": TRAIN_METRIC, "value": round(cfg.T / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) x and dy, N(0,1/d) weights, random init)",
+        "config": {"workload": f"{cfg.name} training step: T={cfg.T} d={cfg.d} E={cfg.E}+1 I={cfg.I} K={cfg.K} "
+                               f"G={cfg.G} M={cfg.M}", "scale_rule": args.scales, "parallelism": "dp1",
+                   "launch": "one CUDA graph of the K steps" if graph is not None else "eager launches",
+                   "l2": "inputs exceed L2 (x, dy, weights and gradients read or written every step), no flush"},
+        "layer_tflops": round((cfg.flops() + bwd_flops) / (ms * 1e-3) / 1e12, 1),
+        "kernels_ms": {n: round(v, 4) for n, v in kt.items()},
+        "roofline": roof,
+        "e2e": {"value": round(cfg.T / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": 2 * cfg.T * d * 2,
+                "d2h_bytes_per_step": cfg.T * d * 2},
+        "gpu_launches": K * (layer.launches_per_forward + layer.launches_per_backward),
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(out), flush=True)
+
+
 def e2e_pipelined(cfg, layer, x, K, hook, binding, T_all):
     """Milliseconds per step of K forwards fed from and drained to pinned host memory."""
     import torch
@@ -402,11 +523,15 @@ def main():
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph of the K steps")
     ap.add_argument("--scales", default="fp32", choices=["fp32", "pow2"],
                     help="pow2: power-of-two 1x128 / 128x128 scales and the block-scaled GEMMs")
+    ap.add_argument("--backward", action="store_true",
+                    help="time a training step (forward, bias update, backward) instead of the forward")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.backward:
+        run_train(args)
     else:
         run_ours(args)
 

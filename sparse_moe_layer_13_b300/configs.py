@@ -74,4 +74,8 @@ CONFIGS = {c.name: c for c in (TINY, MID, FULL, DECODE, SKEW)}
 # experts and 4096 tokens: the same per-tile GEMM behaviour as the full-width
 # prefill in about 3 GB of device memory, for kernel profiles.
 FULLWIDTH_SMALL = MoEConfig("fullwidth_small", T=4096, d=7168, E=32, I=2048, K=8, G=8, M=4, gk=2, seed=5)
-PROFILE_CONFIGS = {FULLWIDTH_SMALL.name: FULLWIDTH_SMALL}
+# Full-width shapes with 16 routed experts and 1024 tokens: 512 rows per expert as in the
+# full-width prefill, about 4 GB of device memory for a training step, for profiles of the
+# backward kernels.
+FULLWIDTH_E16 = MoEConfig("fullwidth_e16", T=1024, d=7168, E=16, I=2048, K=8, G=8, M=4, gk=2, seed=6)
+PROFILE_CONFIGS = {c.name: c for c in (FULLWIDTH_SMALL, FULLWIDTH_E16)}

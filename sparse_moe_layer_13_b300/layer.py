@@ -166,7 +166,7 @@ class MoELayer:
             B.bias_update(c.E, c.T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
         return y
 
-    def backward(self, x: torch.Tensor, dy: torch.Tensor) -> dict:
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, events=None) -> dict:
         """Gradients of the last forward (on x) for upstream gradient dy (bf16 [T][d]),
         with the chosen experts held fixed, on the current stream.
 
@@ -181,7 +181,9 @@ class MoELayer:
           dW2T f32  [E+1][I][d]   the down projection's gradient, transposed
           dgate, dz f32 [T][K]    gate and router-logit gradients
         Every FP8 GEMM runs on the FP32-scale tensor-core kernels under the
-        layer's scale rule.
+        layer's scale rule. events, if given, maps "dgrad2", "recompute",
+        "dgrad1", "wgrad2", "wgrad1" to (start, end) event pairs recorded
+        around those GEMMs.
         """
         c = self.cfg
         if not getattr(self.w, "backward", False):
@@ -197,18 +199,34 @@ class MoELayer:
         B.combine_backward(c, dy, self.out, ro, self.gate, bw["dOq"], bw["dOs"], bw["row_gate"], bw["dgate"], rule)
         B.route_backward(c, self.idx, bw["dgate"], self.ws, bw["dz"], self.logit_offset)
         B.router_wgrad(c, x, offs[:E + 1], st, ro, bw["dz"], bw["dWr"])
+        ev = events or {}
+
+        def mark(name, i):
+            if name in ev:
+                ev[name][i].record()
+
+        mark("dgrad2", 0)
         B.grouped_gemm_fp8(offs, bw["dOq"], bw["dOs"], self.w.q2T, self.w.s2T, B.MOE_EPI_F32, bw["dh"])
+        mark("dgrad2", 1)
+        mark("recompute", 0)
         B.grouped_gemm_fp8(offs, self.xq_perm, self.xs_perm, self.w.q13, self.w.s13, B.MOE_EPI_GATEUP_F32, bw["ab"])
+        mark("recompute", 1)
         B.swiglu_backward(bw["ab"], bw["dh"], bw["dabq"], bw["dabs"], rule)
+        mark("dgrad1", 0)
         B.grouped_gemm_fp8(offs, bw["dabq"], bw["dabs"], self.w.q13T, self.w.s13T, B.MOE_EPI_BF16_F32_LAST,
                            bw["dxr"], bw["dxs"])
+        mark("dgrad1", 1)
         B.dx_combine(c, bw["dxr"], bw["dxs"], ro, self.idx, bw["dz"], self.Wr, bw["dx"])
         B.quant_128x1(offs, R, d, rule, bw["oT"], bw["oS"], bf16_rows=(dy, st, bw["row_gate"]))
         B.quant_128x1(offs, R, I, rule, bw["hT"], bw["hS"], fp8=(self.hq, self.hs))
         B.quant_128x1(offs, R, 2 * I, rule, bw["gT"], bw["gS"], f32=bw["ab"])
         B.quant_128x1(offs, R, d, rule, bw["xT"], bw["xS"], fp8=(self.xq_perm, self.xs_perm))
+        mark("wgrad2", 0)
         B.grouped_wgrad_fp8(offs, R, bw["hT"], bw["hS"], bw["oT"], bw["oS"], bw["dW2T"])
+        mark("wgrad2", 1)
+        mark("wgrad1", 0)
         B.grouped_wgrad_fp8(offs, R, bw["gT"], bw["gS"], bw["xT"], bw["xS"], bw["dW13"])
+        mark("wgrad1", 1)
         return {k: bw[k] for k in ("dx", "dWr", "dW13", "dW2T", "dgate", "dz")}
 
     # library kernel launches per backward: combine 1, route 1, router weight 1, GEMMs 5,
