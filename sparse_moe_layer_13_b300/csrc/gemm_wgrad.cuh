@@ -9,10 +9,12 @@
 // transposed operands (quant_128x1_kernel's layout); D is FP32 [groups][M][N].
 //
 // Same warp roles as the grouped forward GEMM: warp 0 TMA producer (operand
-// tiles 128x128 and 256x128 into a 4-stage ring; the chunk's 128 + 256 scale
-// values by bulk copy into an 8-slot scale ring), warp 1 MMA issuer
+// tiles 128x128 and 256x128 into a 3-stage ring; the chunk's 128 + 256 scale
+// values by bulk copy into a 4-slot scale ring), warp 1 MMA issuer
 // (tcgen05.mma M128 N256 K32 into two TMEM chunk accumulators), warps 4..11
-// epilogue (row rit of the tile, 128 columns: acc += partial * sa[rit] * sb[n]).
+// epilogue (row rit of the tile, 128 columns: acc += partial * sa[rit] * sb[n];
+// the finished tile leaves through shared memory by TMA stores of 32x32 boxes,
+// since direct stores of 32 rows per warp instruction tie up L1).
 // Tiles: groups in reverse order (the shared expert, last and largest, first),
 // then row tile, then column tile; CTA c takes tiles c, c + gridDim.x, ...
 // A group with no rows gets zero tiles.
@@ -30,13 +32,16 @@ using gemm::BN;
 using gemm::A_BYTES;
 using gemm::B_BYTES;
 using gemm::STAGE_BYTES;
-using gemm::STAGES;
 using gemm::NUM_THREADS;
 using gemm::kRegsEpilogue;
 using gemm::kRegsProducer;
 using gemm::TMEM_COLS;
 using gemm::IDESC;
-constexpr int SSLOTS = 8;
+constexpr int STAGES = 3;                 // operand ring (few K chunks per tile; room for the store staging)
+constexpr int SSLOTS = 4;                 // scale ring
+constexpr int OUT_BOX = 32;               // output box: 32 rows x 32 FP32 columns, 128-byte swizzle
+constexpr int OUT_BOX_BYTES = OUT_BOX * OUT_BOX * 4;
+constexpr int OUT_STAGE_BYTES = 8 * 2 * OUT_BOX_BYTES;   // two boxes per epilogue warp
 constexpr int MAX_GROUPS = 1025;
 constexpr uint32_t SCALE_BYTES = (BM + BN) * sizeof(float);
 
@@ -56,7 +61,7 @@ struct Smem {
     alignas(16) float sb[SSLOTS][BN];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Smem);
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OUT_STAGE_BYTES + sizeof(Smem);
 static_assert(SMEM_BYTES <= 227 * 1024, "more shared memory than a CTA may have");
 
 struct Params {
@@ -81,12 +86,14 @@ __device__ __forceinline__ void decode(int tile, int groups, int mtn, int ntn, i
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmOut, Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = base;
     uint8_t* sB = base + STAGES * A_BYTES;
-    Smem& s = *reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES);
+    uint8_t* sOut = base + STAGES * STAGE_BYTES;                    // 1024-byte aligned
+    Smem& s = *reinterpret_cast<Smem*>(sOut + OUT_STAGE_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
@@ -104,6 +111,7 @@ grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmOut);
     }
     if (warp == 1) {
         tmem_alloc(&s.tmem_base, TMEM_COLS);
@@ -211,7 +219,7 @@ grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         const int q = warp & 3;              // TMEM lane quadrant this warp may access
         const int half = ew >> 2;            // column half of the 256-wide tile
         const int rit = q * 32 + static_cast<int>(lane);
-        uint32_t it = 0;
+        uint32_t it = 0, nbox = 0;
         bool ok = run;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             int g, mt, nt;
@@ -265,14 +273,34 @@ grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             }
             if (!ok) break;
             float* acc = reinterpret_cast<float*>(acc2);
-            float* dst = p.out + (static_cast<int64_t>(g) * p.M + mt * BM + rit) * p.N + nt * BN + half * 128;
+            // 4 boxes of 32 columns: the warp's 32 rows go to shared memory in the 128-byte
+            // swizzled box layout (16-byte chunk c of row r at chunk c ^ (r % 8): a quarter warp
+            // covers all banks), then one lane stores the box with TMA. Two boxes alternate; a box
+            // is rewritten only after the store issued two boxes earlier has read it.
+            const int y = g * p.M + mt * BM + q * 32;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                st_v8_b32(dst + 8 * i, __float_as_uint(acc[8 * i]), __float_as_uint(acc[8 * i + 1]),
-                          __float_as_uint(acc[8 * i + 2]), __float_as_uint(acc[8 * i + 3]),
-                          __float_as_uint(acc[8 * i + 4]), __float_as_uint(acc[8 * i + 5]),
-                          __float_as_uint(acc[8 * i + 6]), __float_as_uint(acc[8 * i + 7]));
+            for (int j = 0; j < 4; ++j, ++nbox) {
+                uint8_t* buf = sOut + (ew * 2 + (nbox & 1u)) * OUT_BOX_BYTES;
+                if (nbox >= 2) {
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+                }
+                const uint32_t row = smem_addr(buf) + lane * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(row + ((c ^ (lane & 7)) << 4), acc[32 * j + 4 * c], acc[32 * j + 4 * c + 1],
+                                 acc[32 * j + 4 * c + 2], acc[32 * j + 4 * c + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmOut, buf, nt * BN + half * 128 + j * 32, y);
+                    bulk_commit();
+                }
+            }
         }
+        // every store has finished with shared memory (and written its box) before the CTA exits
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
     }
 
     tc_fence_before();

@@ -121,6 +121,19 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D FP32 matrix [outer][inner], box [32][32 elements] (128 bytes), 128-byte swizzle.
+bool make_map_f32_box32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D K-major bf16 matrix [outer][inner], box [box_outer][64 elements], 128-byte swizzle.
 bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
     EncodeTiledFn fn = encode_fn();
@@ -767,9 +780,10 @@ moe_status moe_grouped_wgrad_fp8(int32_t groups, const int32_t* offsets, int64_t
                    ? MOE_OK
                    : MOE_ERR_CUDA;
     }
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, to;
     if (!make_map_u8(&ta, AT, static_cast<uint64_t>(width), static_cast<uint64_t>(M), gemm::BM)) return MOE_ERR_CUDA;
     if (!make_map_u8(&tb, BT, static_cast<uint64_t>(width), static_cast<uint64_t>(N), gemm::BN)) return MOE_ERR_CUDA;
+    if (!make_map_f32_box32(&to, out, static_cast<uint64_t>(N), static_cast<uint64_t>(groups) * M)) return MOE_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(wgrad::grouped_wgrad_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -780,7 +794,7 @@ moe_status moe_grouped_wgrad_fp8(int32_t groups, const int32_t* offsets, int64_t
     wgrad::Params p{offsets, groups, rows, width / 128, M, N, saT, sbT, out};
     const int64_t tiles = static_cast<int64_t>(groups) * (M / gemm::BM) * (N / gemm::BN);
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), tiles));
-    wgrad::grouped_wgrad_fp8_kernel<<<grid, gemm::NUM_THREADS, wgrad::SMEM_BYTES, as_stream(stream)>>>(ta, tb, p);
+    wgrad::grouped_wgrad_fp8_kernel<<<grid, gemm::NUM_THREADS, wgrad::SMEM_BYTES, as_stream(stream)>>>(ta, tb, to, p);
     return launch_status();
 }
 
