@@ -73,6 +73,21 @@ struct Smem {
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(Smem);
 static_assert(SMEM_BYTES <= 227 * 1024, "more shared memory than a CTA may have");
 
+// The all-FP32 epilogues (the backward pass's data-gradient and recomputation GEMMs) send
+// their tiles out through shared memory by TMA stores: per epilogue warp two 2 KB boxes of
+// 32 rows x 16 FP32 (64-byte swizzle), which takes a 3-stage operand ring to fit.
+constexpr int OUT_BOX_COLS = 16;
+constexpr int OUT_BOX_BYTES = 32 * OUT_BOX_COLS * 4;
+constexpr int OUT_STAGE_BYTES = 8 * 2 * OUT_BOX_BYTES;
+template <int EPI>
+struct EpiCfg {
+    static constexpr bool kTmaOut = EPI == MOE_EPI_F32 || EPI == MOE_EPI_GATEUP_F32;
+    static constexpr int kStages = kTmaOut ? 3 : STAGES;
+    static constexpr int kOutBytes = kTmaOut ? OUT_STAGE_BYTES : 0;
+    static constexpr size_t kSmem = 1024 + kStages * STAGE_BYTES + kOutBytes + sizeof(Smem);
+};
+static_assert(EpiCfg<MOE_EPI_F32>::kSmem <= 227 * 1024, "more shared memory than a CTA may have");
+
 struct Params {
     const int32_t* offsets;
     int32_t groups;
@@ -210,16 +225,64 @@ __device__ __forceinline__ bool store_tile(float* acc, const Params& p, SmemT& s
     return true;
 }
 
+// The finished FP32 tile accumulator of this thread (row rit of the tile, 128 columns of
+// column half `half`) to the FP32 output through shared memory: the warp's 32 rows go out
+// as 8 TMA boxes of 32 rows x 16 columns, written into one of the warp's two staging
+// buffers in the 64-byte swizzled layout (16-byte chunk c of row r at chunk c ^ ((r/2) % 4),
+// which spreads a quarter warp over all banks). A buffer is rewritten only after the store
+// issued two boxes earlier has read it. A warp whose 32 rows are not all in the tile's
+// group stores its valid rows directly (a box would overwrite the next group's rows).
+__device__ __forceinline__ void store_tile_tma(const float* acc, const Params& p, const CUtensorMap* tmOut,
+                                               uint8_t* sOut, const TileInfo& t, int rit, int half, int ew, int q,
+                                               uint32_t lane, uint32_t& nbox) {
+    const int64_t row0 = static_cast<int64_t>(t.row0) + q * 32;
+    const int col0 = t.nt * BN + half * 128;
+    if (q * 32 + 32 > t.m_valid) {                       // warp-uniform
+        if (rit < t.m_valid) {
+            float* dst = static_cast<float*>(p.out) + (row0 + lane) * p.N + col0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                st_v8_b32(dst + 8 * i, __float_as_uint(acc[8 * i]), __float_as_uint(acc[8 * i + 1]),
+                          __float_as_uint(acc[8 * i + 2]), __float_as_uint(acc[8 * i + 3]),
+                          __float_as_uint(acc[8 * i + 4]), __float_as_uint(acc[8 * i + 5]),
+                          __float_as_uint(acc[8 * i + 6]), __float_as_uint(acc[8 * i + 7]));
+        }
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 128 / OUT_BOX_COLS; ++j, ++nbox) {
+        uint8_t* buf = sOut + (ew * 2 + (nbox & 1u)) * OUT_BOX_BYTES;
+        if (nbox >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+        }
+        const uint32_t row = smem_addr(buf) + lane * (OUT_BOX_COLS * 4);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            st_shared_v4(row + ((c ^ ((lane >> 1) & 3u)) << 4), acc[16 * j + 4 * c], acc[16 * j + 4 * c + 1],
+                         acc[16 * j + 4 * c + 2], acc[16 * j + 4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmOut, buf, col0 + OUT_BOX_COLS * j, static_cast<int32_t>(row0));
+            bulk_commit();
+        }
+    }
+}
+
 // GATHER: A rows are fetched by index (TMA gather4, four rows per copy)
 // instead of as one 128-row tile.
 template <int EPI, bool GATHER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut, Params p) {
+    constexpr int STAGES = EpiCfg<EPI>::kStages;     // operand ring of this epilogue
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = base;
     uint8_t* sB = base + STAGES * A_BYTES;
-    Smem& s = *reinterpret_cast<Smem*>(base + STAGES * STAGE_BYTES);
+    uint8_t* sOut = base + STAGES * STAGE_BYTES;     // TMA-store staging (all-FP32 epilogues)
+    Smem& s = *reinterpret_cast<Smem*>(sOut + EpiCfg<EPI>::kOutBytes);
 
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
@@ -238,6 +301,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (EpiCfg<EPI>::kTmaOut) tma_prefetch_desc(&tmOut);
     }
     if (warp == 1) {
         tmem_alloc(&s.tmem_base, TMEM_COLS);
@@ -404,7 +468,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         };
         // (the all-FP32 store epilogue keeps per-tile copies: the look-ahead state makes it spill)
         const bool ahead = EPI != MOE_EPI_F32 && EPI != MOE_EPI_GATEUP_F32 && nkc >= 3;
-        uint32_t it = 0, tcount = 0;
+        uint32_t it = 0, tcount = 0, nbox = 0;
         bool ok = true;
         ScaleRows cur{0, 0}, nxt{0, 0};
         if (ahead && static_cast<int>(blockIdx.x) < total) {
@@ -477,10 +541,17 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             }
             float* acc = reinterpret_cast<float*>(acc2);
             if (!ok) break;
-            if (!store_tile<EPI, false>(acc, p, s, t, groups, last_start, rit, half, ew, q, lane, tcount, abort)) break;
+            if constexpr (EpiCfg<EPI>::kTmaOut)
+                store_tile_tma(acc, p, &tmOut, sOut, t, rit, half, ew, q, lane, nbox);
+            else if (!store_tile<EPI, false>(acc, p, s, t, groups, last_start, rit, half, ew, q, lane, tcount, abort))
+                break;
             cur = nxt;
         }
         cp_async_wait<0>();          // no scale copy may still target shared memory at exit
+        if (EpiCfg<EPI>::kTmaOut) {  // every box store has read its buffer and landed
+            if (lane == 0) bulk_wait<0>();
+            __syncwarp();
+        }
     }
 
     tc_fence_before();

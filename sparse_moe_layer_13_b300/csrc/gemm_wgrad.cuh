@@ -237,34 +237,27 @@ grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 tc_fence_after();
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * BN + half * 128;
                 const float2 sa2 = make_float2(sav, sav);
+                // four steps of 32 columns (half * 128 + r * 32 ..): fewer live registers than two of 64
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(taddr + r * 64, v0);
-                    tmem_ld32(taddr + r * 64 + 32, v1);
+                for (int r = 0; r < 4; ++r) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + r * 32, v);
                     tmem_ld_wait();
-                    tmem_reg_fence(v0);
-                    tmem_reg_fence(v1);
-                    if (r == 1) {                // every value of the chunk is in registers now
+                    tmem_reg_fence(v);
+                    if (r == 3) {                // every value of the chunk is in registers now
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&s.tempty[b]);
                     }
-                    // columns r*64 + 4i .. +3 (from v0) and r*64 + 32 + 4i .. +3 (from v1)
-                    const float4* sbp = reinterpret_cast<const float4*>(&s.sb[ss][half * 128 + r * 64]);
+                    const float4* sbp = reinterpret_cast<const float4*>(&s.sb[ss][half * 128 + r * 32]);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float4 w0 = sbp[i], w1 = sbp[8 + i];
-                        float2* a0 = &acc2[r * 32 + 2 * i];
-                        float2* a1 = &acc2[r * 32 + 16 + 2 * i];
-                        a0[0] = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(v0[4 * i]), __uint_as_float(v0[4 * i + 1])),
-                                                      make_float2(w0.x, w0.y)), sa2, a0[0]);
-                        a0[1] = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(v0[4 * i + 2]), __uint_as_float(v0[4 * i + 3])),
-                                                      make_float2(w0.z, w0.w)), sa2, a0[1]);
-                        a1[0] = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(v1[4 * i]), __uint_as_float(v1[4 * i + 1])),
-                                                      make_float2(w1.x, w1.y)), sa2, a1[0]);
-                        a1[1] = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(v1[4 * i + 2]), __uint_as_float(v1[4 * i + 3])),
-                                                      make_float2(w1.z, w1.w)), sa2, a1[1]);
+                        const float4 w = sbp[i];
+                        float2* a = &acc2[r * 16 + 2 * i];
+                        a[0] = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])),
+                                                     make_float2(w.x, w.y)), sa2, a[0]);
+                        a[1] = __ffma2_rn(__fmul2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                                                     make_float2(w.z, w.w)), sa2, a[1]);
                     }
                 }
                 // every scale of this chunk has been read

@@ -121,17 +121,18 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D FP32 matrix [outer][inner], box [32][32 elements] (128 bytes), 128-byte swizzle.
-bool make_map_f32_box32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+// 2-D FP32 matrix [outer][inner] for TMA stores of boxes of 32 rows x box_cols elements:
+// box_cols 32 (128 bytes, 128-byte swizzle) or 16 (64 bytes, 64-byte swizzle).
+bool make_map_f32_box(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_cols) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * 4};
-    cuuint32_t box[2] = {32, 32};
+    cuuint32_t box[2] = {box_cols, 32};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D K-major bf16 matrix [outer][inner], box [box_outer][64 elements], 128-byte swizzle.
@@ -173,29 +174,32 @@ void launch_select(const moe_config* c, const float* z, int ks, const float* off
     else launch_select_e<32>(c, z, ks, off, bias, idx, gate, grid, smem, st);
 }
 
+// to: the FP32 output's tensor map for the all-FP32 epilogues (unused by the others)
 template <int EPI, bool GATHER>
-moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p, int64_t tiles_max,
-                       cudaStream_t st) {
+moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const gemm::Params& p,
+                       int64_t tiles_max, cudaStream_t st) {
+    constexpr size_t smem = gemm::EpiCfg<EPI>::kSmem;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(gemm::grouped_gemm_fp8_kernel<EPI, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(gemm::SMEM_BYTES)) != cudaSuccess)
+                                 static_cast<int>(smem)) != cudaSuccess)
             return MOE_ERR_CUDA;
         attr_set = true;
     }
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_max, 1)));
-    gemm::grouped_gemm_fp8_kernel<EPI, GATHER><<<grid, gemm::NUM_THREADS, gemm::SMEM_BYTES, st>>>(ta, tb, p);
+    gemm::grouped_gemm_fp8_kernel<EPI, GATHER><<<grid, gemm::NUM_THREADS, smem, st>>>(ta, tb, to, p);
     return launch_status();
 }
 
 template <bool GATHER>
-moe_status launch_gemm_epi(int32_t epilogue, const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p,
-                           int64_t tiles_max, cudaStream_t st) {
-    if (epilogue == MOE_EPI_BF16) return launch_gemm<MOE_EPI_BF16, GATHER>(ta, tb, p, tiles_max, st);
-    if (epilogue == MOE_EPI_F32) return launch_gemm<MOE_EPI_F32, GATHER>(ta, tb, p, tiles_max, st);
-    if (epilogue == MOE_EPI_BF16_F32_LAST) return launch_gemm<MOE_EPI_BF16_F32_LAST, GATHER>(ta, tb, p, tiles_max, st);
-    if (epilogue == MOE_EPI_GATEUP_F32) return launch_gemm<MOE_EPI_GATEUP_F32, GATHER>(ta, tb, p, tiles_max, st);
-    return launch_gemm<MOE_EPI_SWIGLU_FP8, GATHER>(ta, tb, p, tiles_max, st);
+moe_status launch_gemm_epi(int32_t epilogue, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                           const gemm::Params& p, int64_t tiles_max, cudaStream_t st) {
+    if (epilogue == MOE_EPI_BF16) return launch_gemm<MOE_EPI_BF16, GATHER>(ta, tb, to, p, tiles_max, st);
+    if (epilogue == MOE_EPI_F32) return launch_gemm<MOE_EPI_F32, GATHER>(ta, tb, to, p, tiles_max, st);
+    if (epilogue == MOE_EPI_BF16_F32_LAST)
+        return launch_gemm<MOE_EPI_BF16_F32_LAST, GATHER>(ta, tb, to, p, tiles_max, st);
+    if (epilogue == MOE_EPI_GATEUP_F32) return launch_gemm<MOE_EPI_GATEUP_F32, GATHER>(ta, tb, to, p, tiles_max, st);
+    return launch_gemm<MOE_EPI_SWIGLU_FP8, GATHER>(ta, tb, to, p, tiles_max, st);
 }
 
 template <int EPI>
@@ -253,8 +257,13 @@ moe_status grouped_gemm(int32_t groups, const int32_t* offsets, int64_t rows, in
         if (epilogue == MOE_EPI_BF16_F32_LAST) return launch_gemm_mx<MOE_EPI_BF16_F32_LAST>(ta, tb, p, tiles_max, st);
         return launch_gemm_mx<MOE_EPI_SWIGLU_FP8>(ta, tb, p, tiles_max, st);
     }
-    if (gather) return launch_gemm_epi<true>(epilogue, ta, tb, p, tiles_max, st);
-    return launch_gemm_epi<false>(epilogue, ta, tb, p, tiles_max, st);
+    CUtensorMap to = ta;       // a placeholder for the epilogues that store directly
+    if (epilogue == MOE_EPI_F32 || epilogue == MOE_EPI_GATEUP_F32) {
+        if (!make_map_f32_box(&to, out, static_cast<uint64_t>(N), static_cast<uint64_t>(rows), gemm::OUT_BOX_COLS))
+            return MOE_ERR_CUDA;
+    }
+    if (gather) return launch_gemm_epi<true>(epilogue, ta, tb, to, p, tiles_max, st);
+    return launch_gemm_epi<false>(epilogue, ta, tb, to, p, tiles_max, st);
 }
 
 const char* kStatusNames[] = {
@@ -783,7 +792,7 @@ moe_status moe_grouped_wgrad_fp8(int32_t groups, const int32_t* offsets, int64_t
     CUtensorMap ta, tb, to;
     if (!make_map_u8(&ta, AT, static_cast<uint64_t>(width), static_cast<uint64_t>(M), gemm::BM)) return MOE_ERR_CUDA;
     if (!make_map_u8(&tb, BT, static_cast<uint64_t>(width), static_cast<uint64_t>(N), gemm::BN)) return MOE_ERR_CUDA;
-    if (!make_map_f32_box32(&to, out, static_cast<uint64_t>(N), static_cast<uint64_t>(groups) * M)) return MOE_ERR_CUDA;
+    if (!make_map_f32_box(&to, out, static_cast<uint64_t>(N), static_cast<uint64_t>(groups) * M, 32)) return MOE_ERR_CUDA;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(wgrad::grouped_wgrad_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
