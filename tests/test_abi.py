@@ -81,3 +81,42 @@ def test_host_side_errors_return_before_launch(lib):
     # workspace too small
     assert lib.moe_permute(ctypes.byref(c), fake, fake, fake, fake, None, fake, fake, fake, fake, fake, 16, None) == 3
     assert lib.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, fake, None, None, 0, None) == 3
+
+
+def test_backward_host_side_errors_return_before_launch(lib):
+    """Every backward entry point rejects bad pointers, enums and shapes on the host."""
+    from sparse_moe_layer_13_b300 import binding
+    from sparse_moe_layer_13_b300.configs import TINY
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    odd = P(0x10001)
+    not32 = P(0x10010)         # 16-byte but not 32-byte aligned
+    c = ctypes.byref(binding.config_c(TINY))
+    # block transpose: null source, ldT < rows, rows not a multiple of 128
+    assert lib.moe_transpose_fp8_blocks(None, fake, 1, 128, 128, fake, fake, 128, 128, None) == 1
+    assert lib.moe_transpose_fp8_blocks(fake, fake, 1, 256, 128, fake, fake, 128, 128, None) == 1
+    assert lib.moe_transpose_fp8_blocks(fake, fake, 1, 100, 128, fake, fake, 128, 128, None) == 2
+    # combine / router backward: bad scale rule, config, workspace, alignment
+    assert lib.moe_combine_backward(c, fake, fake, fake, fake, 5, fake, fake, fake, fake, None) == 1
+    assert lib.moe_combine_backward(None, fake, fake, fake, fake, 0, fake, fake, fake, fake, None) == 1
+    assert lib.moe_route_backward(c, None, fake, fake, fake, None, 0, None) == 3
+    assert lib.moe_router_wgrad(c, odd, fake, fake, fake, fake, fake, None) == 1
+    assert lib.moe_dx_combine(c, fake, fake, fake, fake, fake, None, fake, None) == 1
+    # SwiGLU backward: ld_dh < I, I not a multiple of 128
+    assert lib.moe_swiglu_backward(4, 256, fake, fake, 128, 0, fake, fake, None) == 1
+    assert lib.moe_swiglu_backward(4, 100, fake, fake, 100, 0, fake, fake, None) == 2
+    # 128x1 quantisers: columns, group count, ldq alignment, source strides
+    assert lib.moe_quant_fp8_128x1_f32(fake, 128, 2, fake, 64, 100, 0, fake, 1024, fake, None) == 2
+    assert lib.moe_quant_fp8_128x1_f32(fake, 128, 2000, fake, 64, 128, 0, fake, 1024, fake, None) == 2
+    assert lib.moe_quant_fp8_128x1_f32(fake, 128, 2, fake, 64, 128, 0, fake, 1000, fake, None) == 1
+    assert lib.moe_quant_fp8_128x1_f32(fake, 128, 2, fake, 64, 128, 3, fake, 1024, fake, None) == 1
+    assert lib.moe_quant_fp8_128x1_fp8(fake, fake, 200, 2, fake, 64, 128, 0, fake, 1024, fake, None) == 1
+    assert lib.moe_quant_fp8_128x1_bf16_rows(fake, 8, 128, None, None, 2, fake, 64, 128, 0, fake, 1024, fake,
+                                            None) == 1
+    # weight-gradient GEMM: M, N tiles, group count, output alignment
+    assert lib.moe_grouped_wgrad_fp8(2, fake, 64, 512, 100, 256, fake, fake, fake, fake, fake, None) == 2
+    assert lib.moe_grouped_wgrad_fp8(2, fake, 64, 512, 128, 128, fake, fake, fake, fake, fake, None) == 2
+    assert lib.moe_grouped_wgrad_fp8(2000, fake, 64, 512, 128, 256, fake, fake, fake, fake, fake, None) == 2
+    assert lib.moe_grouped_wgrad_fp8(2, fake, 64, 512, 128, 256, fake, fake, fake, fake, not32, None) == 1
+    # the gate/up FP32 epilogue has no block-scaled variant
+    assert lib.moe_grouped_gemm_fp8_mx(4, fake, 100, 256, 256, fake, fake, fake, fake, 4, fake, None, None) == 2
