@@ -386,37 +386,82 @@ quant_128x1_kernel(QSrc src, int64_t rows, int cols, int groups, const int32_t* 
     const int64_t row0 = __ldg(offsets + g) + static_cast<int64_t>(slot - prefix[g]) * 128;
     const int m = static_cast<int>(min(static_cast<int64_t>(128), __ldg(offsets + g + 1) - row0));
     const int c0 = blockIdx.y * 128;
-    // load: thread -> rows tid/32 + 8i, columns 4 * (tid % 32) .. + 3
-    const int tr = tid >> 5, tc = (tid & 31) * 4;
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-        const int rr = tr + 8 * i;
-        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (rr < m) {
-            const int64_t r = row0 + rr;
-            if (SRC == SRC_F32) {
-                const float4 f = __ldg(reinterpret_cast<const float4*>(src.f32 + r * src.ld + c0 + tc));
-                v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-            } else if (SRC == SRC_FP8) {
-                const uint32_t cw = __ldg(reinterpret_cast<const uint32_t*>(src.q8 + r * src.ld + c0 + tc));
-                const float sc = __ldg(src.s8 + r * src.ld_s + (c0 >> 7));
-                const float2 lo2 = e4m3x2_to_f32(cw & 0xFFFFu), hi2 = e4m3x2_to_f32(cw >> 16);
-                v[0] = __fmul_rn(lo2.x, sc); v[1] = __fmul_rn(lo2.y, sc);
-                v[2] = __fmul_rn(hi2.x, sc); v[3] = __fmul_rn(hi2.y, sc);
-            } else {
-                int64_t t = __ldg(src.map + r);
-                if (t < 0 || t >= src.src_rows) { set_status(MOE_ERR_DEVICE_CHECK); t = 0; }
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(src.bf16 + t * src.ld + c0 + tc));
-                v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-                if (src.mult != nullptr) {
-                    const float mu = __ldg(src.mult + r);
+    // load: 16-byte loads, all of a thread's issued before the tile is written (the kernel
+    // is bound by HBM latency x bytes in flight). Rows past the group's end are zeros.
+    if (SRC == SRC_F32) {
+        // thread -> rows tid/32 + 8i (i < 16), columns 4 * (tid % 32) .. + 3
+        const int tr = tid >> 5, tc = (tid & 31) * 4;
+        float4 f[16];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(mu, v[j]);
-                }
+        for (int i = 0; i < 16; ++i) {
+            const int rr = tr + 8 * i;
+            f[i] = rr < m ? __ldg(reinterpret_cast<const float4*>(src.f32 + (row0 + rr) * src.ld + c0 + tc))
+                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float* d = tile + (tr + 8 * i) * 129 + tc;
+            d[0] = f[i].x; d[1] = f[i].y; d[2] = f[i].z; d[3] = f[i].w;
+        }
+    } else if (SRC == SRC_FP8) {
+        // thread -> rows tid/8 + 32i (i < 4), columns 16 * (tid % 8) .. + 15 (one 1x128 scale per row)
+        const int tr = tid >> 3, tc = (tid & 7) * 16;
+        uint4 w[4];
+        float sc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = tr + 32 * i;
+            w[i] = make_uint4(0, 0, 0, 0);
+            sc[i] = 0.0f;
+            if (rr < m) {
+                const int64_t r = row0 + rr;
+                w[i] = __ldg(reinterpret_cast<const uint4*>(src.q8 + r * src.ld + c0 + tc));
+                sc[i] = __ldg(src.s8 + r * src.ld_s + (c0 >> 7));
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tile[rr * 129 + tc + j] = v[j];
+        for (int i = 0; i < 4; ++i) {
+            float* d = tile + (tr + 32 * i) * 129 + tc;
+            const uint32_t cw[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 lo2 = e4m3x2_to_f32(cw[k] & 0xFFFFu), hi2 = e4m3x2_to_f32(cw[k] >> 16);
+                d[4 * k + 0] = __fmul_rn(lo2.x, sc[i]);
+                d[4 * k + 1] = __fmul_rn(lo2.y, sc[i]);
+                d[4 * k + 2] = __fmul_rn(hi2.x, sc[i]);
+                d[4 * k + 3] = __fmul_rn(hi2.y, sc[i]);
+            }
+        }
+    } else {
+        // thread -> rows tid/16 + 16i (i < 8), columns 8 * (tid % 16) .. + 7
+        const int tr = tid >> 4, tc = (tid & 15) * 8;
+        uint4 w[8];
+        float mu[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rr = tr + 16 * i;
+            w[i] = make_uint4(0, 0, 0, 0);
+            mu[i] = 1.0f;
+            if (rr < m) {
+                const int64_t r = row0 + rr;
+                int64_t t = __ldg(src.map + r);
+                if (t < 0 || t >= src.src_rows) { set_status(MOE_ERR_DEVICE_CHECK); t = 0; }
+                w[i] = __ldg(reinterpret_cast<const uint4*>(src.bf16 + t * src.ld + c0 + tc));
+                if (src.mult != nullptr) mu[i] = __ldg(src.mult + r);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float* d = tile + (tr + 16 * i) * 129 + tc;
+            const uint32_t u[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float lo = bf16_lo(u[k]), hi = bf16_hi(u[k]);
+                if (src.mult != nullptr) { lo = __fmul_rn(mu[i], lo); hi = __fmul_rn(mu[i], hi); }
+                d[2 * k] = lo;
+                d[2 * k + 1] = hi;
+            }
+        }
     }
     __syncthreads();
     // column pass: thread -> column tid % 128, rows 64 * (tid / 128) .. + 63
