@@ -1,4 +1,4 @@
-"""FP64 CPU oracle for the DeepSeekMoE layer forward.
+"""FP64 CPU oracle for the DeepSeekMoE layer (forward and backward).
 
 TEST INFRASTRUCTURE ONLY. This package is a plain, slow, obviously correct
 restatement of what the layer computes, used to check the CUDA library.
@@ -28,11 +28,15 @@ Passages followed (page title, section):
 Modules: e4m3 (format codec), quant (block quantisation), route (affinity,
 group-limited selection, gates), permute (histogram and stable grouping
 by expert), ffn (scaled FP8 contraction, SwiGLU expert), layer (whole
-forward, combine, bias update).
+forward, combine, bias update), balance (sequence-wise balance loss),
+backward (the layer's gradients with the expert choice held fixed, FP8
+data and weight gradients, and the flags of quantised elements near an
+E4M3 rounding midpoint).
 
 Parity status: every function is pinned by tests under tests/ (closed
 forms, exhaustive format checks, brute force on tiny inputs, library
-special cases). The pages give no error bound or worked example for the
-layer output itself, so the output tolerance is the one the task states,
-not a number from the pages.
+special cases; the backward's gradients against finite differences). The
+pages give no error bound or worked example for the layer output itself, so
+the output tolerance is the one stated for the layer, not a number from the
+pages; the gradients' tolerances are derived from the arithmetic.
 """
