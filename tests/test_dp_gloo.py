@@ -1,6 +1,8 @@
-"""Data-parallel exchange on CPU: two gloo ranks each route half of a batch
-with the oracle, sum their expert loads with the package's all-reduce, and
-must reach the same bias update as one process that sees the whole batch."""
+"""Data-parallel exchanges on CPU (two gloo ranks, each with half of a batch):
+the expert loads summed by the package's all-reduce must give the bias update
+of one process that sees the whole batch, and the weight gradients summed by
+its gradient all-reduce must equal the whole batch's (the oracle's exact
+float64 gradients, quantisation off)."""
 import os
 import socket
 
@@ -58,3 +60,60 @@ def test_two_rank_load_allreduce_matches_single_process():
     want = np.concatenate([c.astype(np.float64), bias_update(b, c, cfg.T, cfg.K, cfg.gamma).astype(np.float64)])
     for r in range(world):
         assert np.array_equal(out[r].numpy(), want)
+
+
+class _GradCfg:
+    T, d, E, I, K, G, M, gk, seed = 32, 128, 8, 64, 2, 4, 2, 2, 23
+
+
+def _grad_case():
+    """Exact oracle gradients of the seeded small layer: per-half weight gradients can be
+    summed only if they are the same function of disjoint tokens."""
+    from oracle.route import affinity, route
+    cfg = _GradCfg()
+    rng = np.random.default_rng(cfg.seed)
+    x = rng.standard_normal((cfg.T, cfg.d))
+    dy = rng.standard_normal((cfg.T, cfg.d))
+    Wr = rng.standard_normal((cfg.E, cfg.d)) / np.sqrt(cfg.d)
+    W = {e: tuple(rng.standard_normal(sh) / np.sqrt(cfg.d) for sh in ((cfg.I, cfg.d), (cfg.I, cfg.d), (cfg.d, cfg.I)))
+         for e in range(cfg.E + 1)}
+    idx, _, _ = route(x, Wr, np.zeros(cfg.E), cfg.G, cfg.M, cfg.K, cfg.gk)
+    s_sel = np.take_along_axis(affinity(x, Wr), idx, axis=1)
+    return cfg, x, dy, Wr, W, idx, s_sel
+
+
+def _weight_grads(rows):
+    from oracle.backward import Quantiser, layer_backward
+    cfg, x, dy, Wr, W, idx, s_sel = _grad_case()
+    sub = type("C", (), {"T": len(rows), "d": cfg.d, "E": cfg.E, "I": cfg.I, "K": cfg.K})()
+    r = layer_backward(sub, x[rows], dy[rows], Wr, idx[rows], s_sel[rows], lambda e: W[e],
+                       wgrad_experts=range(cfg.E + 1), router_experts=range(cfg.E), Q=Quantiser(on=False),
+                       xd=x[rows])
+    parts = [r["dWr"].get(e, np.zeros(cfg.d)) for e in range(cfg.E)]
+    for e in range(cfg.E + 1):
+        if e in r["dW"]:
+            parts += [m.ravel() for m in r["dW"][e][:3]]
+        else:                      # an expert none of these tokens chose
+            parts += [np.zeros(cfg.I * cfg.d)] * 3
+    return np.concatenate([np.ravel(p) for p in parts])
+
+
+def _grad_rank(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from sparse_moe_layer_13_b300 import dp
+    half = _GradCfg.T // world
+    g = torch.from_numpy(_weight_grads(np.arange(rank * half, (rank + 1) * half)))
+    dp.allreduce_grads([g])
+    out[rank] = g
+    dist.destroy_process_group()
+
+
+def test_two_rank_weight_gradient_allreduce_matches_single_process():
+    world = 2
+    want = _weight_grads(np.arange(_GradCfg.T))
+    out = torch.zeros(world, want.size, dtype=torch.float64).share_memory_()
+    mp.spawn(_grad_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+    for r in range(world):
+        np.testing.assert_allclose(out[r].numpy(), want, rtol=1e-10, atol=1e-12)
