@@ -376,7 +376,53 @@ def run_train(args):
         "gpu_launches": K * (layer.launches_per_forward + layer.launches_per_backward),
         "clocks": clocks.summary(),
     }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_train(cfg, n_tokens=args.cpu_tokens)
     print(json.dumps(out), flush=True)
+
+
+def cpu_baseline_train(cfg, n_tokens: int):
+    """The FP64 oracle's training step as it stands, on a sample of n_tokens tokens: the
+    layer forward of the sample and its backward down to the input gradient (the expert
+    rows of the sampled tokens, router gradient included; weight gradients, which sum
+    over every row of an expert, are not in the sample). Weight quantisation untimed."""
+    import numpy as np
+    import torch
+
+    from oracle.backward import dequant_expert, layer_backward
+    from oracle.layer import Layer
+    from oracle.parallel import quantize_experts
+    from oracle.route import affinity, route as oracle_route
+    from sparse_moe_layer_13_b300 import inputs
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = inputs.gen_x(cfg, dev).float().cpu().numpy()
+    dy = inputs.gen_dy(cfg, dev).float().cpu().numpy()
+    Wr = inputs.gen_router(cfg, dev).cpu().numpy()
+    b = inputs.gen_bias(cfg, dev).cpu().numpy()
+    rng = np.random.default_rng(4321)
+    tok = np.sort(rng.choice(cfg.T, n_tokens, replace=False))
+    idx, _, _ = oracle_route(x[tok], Wr, b, cfg.G, cfg.M, cfg.K, cfg.gk)
+    need = sorted(set(idx.ravel().tolist()) | {cfg.E})
+    ex = quantize_experts((e, *(w.cpu().numpy() for w in inputs.gen_expert(cfg, e, dev))) for e in need)
+    deq = {e: dequant_expert(w) for e, w in ex.items()}
+    layer = Layer(cfg, Wr, b, None, experts=ex)
+    sub = type("Sample", (), {"T": n_tokens, "d": cfg.d, "E": cfg.E, "I": cfg.I, "K": cfg.K})()
+    t = time.perf_counter()
+    fwd = layer.forward(x[tok])
+    s_sel = np.take_along_axis(affinity(x[tok], Wr), fwd["idx"], axis=1)
+    layer_backward(sub, x[tok], dy[tok], Wr, fwd["idx"], s_sel, lambda e: deq[e], tokens=range(n_tokens))
+    dt = time.perf_counter() - t
+    try:
+        from threadpoolctl import threadpool_info
+        blas = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except ImportError:
+        blas = int(os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or os.cpu_count())
+    return {"value": round(n_tokens / dt, 4), "unit": UNIT, "cores": blas, "kind": "oracle",
+            "sample": f"{n_tokens} tokens of the {cfg.name} batch: layer forward and backward to the input "
+                      f"gradient (router gradient included, weight gradients not) in FP64; weight "
+                      f"quantisation untimed",
+            "host_cpus": os.cpu_count()}
 
 
 def e2e_pipelined(cfg, layer, x, K, hook, binding, T_all):
