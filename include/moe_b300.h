@@ -248,7 +248,10 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx,
  * routine.
  * The first call on each device looks up the array's device address with
  * cudaGetSymbolAddress (that device must be current) and caches it; make that
- * first call before any stream capture.
+ * first call before any stream capture. The cache assumes the device's
+ * primary context lives as long as the process: after cudaDeviceReset (or
+ * any teardown of the primary context) the cached address may be stale, so
+ * a process that resets a device must not call this entry point afterwards.
  * All calls share the one array: two calls that overlap on the GPU (e.g. on
  * different streams without ordering between them) race and give wrong
  * results. Each call writes every scratch entry it reads, so what an

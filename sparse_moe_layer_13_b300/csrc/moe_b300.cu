@@ -3,6 +3,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "backward.cuh"
@@ -42,14 +43,28 @@ moe_status check_config(const moe_config* c) {
     return MOE_OK;
 }
 
+// Raises the dynamic shared-memory limit of kernel `fn` to `bytes` once per
+// device: the attribute belongs to the device's context, so each device that
+// launches the kernel needs its own call. `done` holds one bit per device
+// ordinal (< 64); setting the attribute twice from racing threads is harmless.
+moe_status smem_attr(const void* fn, size_t bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return MOE_OK;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    done.fetch_or(bit, std::memory_order_release);
+    return MOE_OK;
+}
+
+// SM count of the current device (queried per call: a cheap attribute read,
+// correct when a process drives devices of different sizes).
 int num_sms() {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 148;
-    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 148;
     return sms;
 }
 
@@ -179,13 +194,9 @@ template <int EPI, bool GATHER>
 moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const gemm::Params& p,
                        int64_t tiles_max, cudaStream_t st) {
     constexpr size_t smem = gemm::EpiCfg<EPI>::kSmem;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm::grouped_gemm_fp8_kernel<EPI, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (smem_attr(reinterpret_cast<const void*>(gemm::grouped_gemm_fp8_kernel<EPI, GATHER>), smem, attr_done) != MOE_OK)
+        return MOE_ERR_CUDA;
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_max, 1)));
     gemm::grouped_gemm_fp8_kernel<EPI, GATHER><<<grid, gemm::NUM_THREADS, smem, st>>>(ta, tb, to, p);
     return launch_status();
@@ -205,13 +216,10 @@ moe_status launch_gemm_epi(int32_t epilogue, const CUtensorMap& ta, const CUtens
 template <int EPI>
 moe_status launch_gemm_mx(const CUtensorMap& ta, const CUtensorMap& tb, const gemm::Params& p, int64_t tiles_max,
                           cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_mx::grouped_gemm_mx_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(gemm_mx::SMEM_BYTES)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (smem_attr(reinterpret_cast<const void*>(gemm_mx::grouped_gemm_mx_kernel<EPI>), gemm_mx::SMEM_BYTES,
+                  attr_done) != MOE_OK)
+        return MOE_ERR_CUDA;
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_max, 1)));
     gemm_mx::grouped_gemm_mx_kernel<EPI><<<grid, gemm::NUM_THREADS, gemm_mx::SMEM_BYTES, st>>>(ta, tb, p);
     return launch_status();
@@ -329,17 +337,12 @@ moe_status launch_q1(const bwd::QSrc& src, int32_t groups, const int32_t* offset
                      int32_t rule, uint8_t* qT, int64_t ldq, float* sT, cudaStream_t st) {
     if (rows == 0 || cols == 0) return MOE_OK;
     const size_t smem = 128 * 129 * sizeof(float) + static_cast<size_t>(groups + 1) * sizeof(int);
-    static bool attr_set[2] = {false, false};
+    static std::atomic<uint64_t> attr_done[2] = {{0}, {0}};
     const int ri = rule == MOE_SCALE_POW2 ? 1 : 0;
-    if (!attr_set[ri]) {
-        const void* fn = rule == MOE_SCALE_POW2 ? reinterpret_cast<const void*>(bwd::quant_128x1_kernel<SRC, true>)
-                                                : reinterpret_cast<const void*>(bwd::quant_128x1_kernel<SRC, false>);
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(128 * 129 * sizeof(float) + (bwd::kQ1MaxGroups + 1) * sizeof(int))) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_set[ri] = true;
-    }
+    const void* fn = rule == MOE_SCALE_POW2 ? reinterpret_cast<const void*>(bwd::quant_128x1_kernel<SRC, true>)
+                                            : reinterpret_cast<const void*>(bwd::quant_128x1_kernel<SRC, false>);
+    if (smem_attr(fn, 128 * 129 * sizeof(float) + (bwd::kQ1MaxGroups + 1) * sizeof(int), attr_done[ri]) != MOE_OK)
+        return MOE_ERR_CUDA;
     const dim3 grid(static_cast<unsigned>(ceil_div(rows, 128) + groups), static_cast<unsigned>(cols / 128));
     if (rule == MOE_SCALE_POW2)
         bwd::quant_128x1_kernel<SRC, true><<<grid, 256, smem, st>>>(src, rows, cols, groups, offsets, qT, ldq, sT);
@@ -397,13 +400,9 @@ moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr, 
     if (!make_map_bf16(&tw, planes, static_cast<uint64_t>(cfg->d), static_cast<uint64_t>(3) * cfg->E,
                        static_cast<uint32_t>(bn)))
         return MOE_ERR_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(rtc::logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(rtc::SMEM_BYTES)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (smem_attr(reinterpret_cast<const void*>(rtc::logits_kernel), rtc::SMEM_BYTES, attr_done) != MOE_OK)
+        return MOE_ERR_CUDA;
     const dim3 lg(static_cast<unsigned>(ceil_div(cfg->T, rtc::BM)), static_cast<unsigned>(ceil_div(cfg->E, rtc::BN_MAX)),
                   static_cast<unsigned>(ks));
     rtc::Params rp{cfg->T, cfg->d, cfg->E, bn, ks, z};
@@ -793,13 +792,10 @@ moe_status moe_grouped_wgrad_fp8(int32_t groups, const int32_t* offsets, int64_t
     if (!make_map_u8(&ta, AT, static_cast<uint64_t>(width), static_cast<uint64_t>(M), gemm::BM)) return MOE_ERR_CUDA;
     if (!make_map_u8(&tb, BT, static_cast<uint64_t>(width), static_cast<uint64_t>(N), gemm::BN)) return MOE_ERR_CUDA;
     if (!make_map_f32_box(&to, out, static_cast<uint64_t>(N), static_cast<uint64_t>(groups) * M, 32)) return MOE_ERR_CUDA;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(wgrad::grouped_wgrad_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(wgrad::SMEM_BYTES)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (smem_attr(reinterpret_cast<const void*>(wgrad::grouped_wgrad_fp8_kernel), wgrad::SMEM_BYTES, attr_done) !=
+        MOE_OK)
+        return MOE_ERR_CUDA;
     wgrad::Params p{offsets, groups, rows, width / 128, M, N, saT, sbT, out};
     const int64_t tiles = static_cast<int64_t>(groups) * (M / gemm::BM) * (N / gemm::BN);
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), tiles));

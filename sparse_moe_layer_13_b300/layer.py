@@ -24,7 +24,7 @@ from __future__ import annotations
 import torch
 
 from . import binding as B
-from . import inputs
+from . import dp, inputs
 from .configs import MoEConfig
 
 
@@ -122,14 +122,19 @@ class MoELayer:
         self.y = z(T, d, dt=torch.bfloat16)
 
     def forward(self, x: torch.Tensor, residual: bool = False, update_bias: bool = True,
-                gamma: float | None = None, counts_hook=None, events=None, out: torch.Tensor | None = None) -> torch.Tensor:
+                gamma: float | None = None, counts_hook=None, load_tokens: int | None = None, events=None,
+                out: torch.Tensor | None = None) -> torch.Tensor:
         """One layer forward on the current stream.
 
-        counts_hook(counts) runs before the bias update (e.g. an all-reduce of
-        the expert load across data-parallel ranks); events, if given, is a
-        dict of name -> (start, end) torch.cuda.Event pairs recorded around
-        the two grouped GEMMs ("gemm1", "gemm2"); out, if given, receives y
-        (bf16 [T][d]) instead of the layer's own buffer.
+        counts_hook(counts) runs before the bias update (e.g. dp.allreduce_load,
+        which sums the expert load over data-parallel ranks); load_tokens is
+        the number of tokens those counts then cover, against whose mean load
+        T*K/E the update judges each expert. It defaults to this layer's T
+        without a hook and to dp.global_tokens(T) with one (every rank of the
+        default group holding T tokens). events, if given, is a dict of
+        name -> (start, end) torch.cuda.Event pairs recorded around the two
+        grouped GEMMs ("gemm1", "gemm2"); out, if given, receives y (bf16
+        [T][d]) instead of the layer's own buffer.
         """
         c = self.cfg
         ev = events or {}
@@ -161,10 +166,21 @@ class MoELayer:
         y = self.y if out is None else out
         B.combine(c, self.out[:TK], self.out_shared, self.perm["row_of"], self.gate, x if residual else None, y)
         if update_bias:
-            if counts_hook is not None:
-                counts_hook(self.counts)
-            B.bias_update(c.E, c.T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
+            self.end_of_step(gamma, counts_hook, load_tokens)
         return y
+
+    def end_of_step(self, gamma: float | None = None, counts_hook=None, load_tokens: int | None = None):
+        """The end-of-step bias update on the last routing's expert load
+        (《DeepSeek-V3 Technical Report》深度解读报告 §2.3): counts_hook(counts)
+        first (e.g. the data-parallel all-reduce), then every bias moves by
+        gamma towards the mean load of the tokens the counts cover."""
+        c = self.cfg
+        if counts_hook is not None:
+            counts_hook(self.counts)
+            T = dp.global_tokens(c.T) if load_tokens is None else load_tokens
+        else:
+            T = c.T if load_tokens is None else load_tokens
+        B.bias_update(c.E, T, c.K, self.counts, c.gamma if gamma is None else gamma, self.bias)
 
     def backward(self, x: torch.Tensor, dy: torch.Tensor, events=None) -> dict:
         """Gradients of the last forward (on x) for upstream gradient dy (bf16 [T][d]),

@@ -117,3 +117,69 @@ def test_two_rank_weight_gradient_allreduce_matches_single_process():
     mp.spawn(_grad_rank, args=(world, _free_port(), out), nprocs=world, join=True)
     for r in range(world):
         np.testing.assert_allclose(out[r].numpy(), want, rtol=1e-10, atol=1e-12)
+
+
+def _layer_step_rank(rank, world, port, out):
+    """MoELayer.end_of_step with the data-parallel load hook, its bias-update
+    call replaced by the oracle's rule on host tensors (no GPU on these ranks):
+    checks which token count the layer hands to the update."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from oracle.layer import bias_update
+    from oracle.permute import histogram
+    from oracle.route import route
+    from sparse_moe_layer_13_b300 import dp, inputs
+    from sparse_moe_layer_13_b300 import layer as layer_mod
+    from sparse_moe_layer_13_b300.configs import MoEConfig
+    full = MoEConfig("dp", T=64, d=128, E=16, I=128, K=4, G=4, M=2, gk=2, seed=21, bias="uniform")
+    cfg = full.with_tokens(full.T // world)
+    x = inputs.gen_x(full).float().numpy()
+    Wr = inputs.gen_router(full).numpy()
+    b = inputs.gen_bias(full).numpy()
+    mine = x[rank * cfg.T:(rank + 1) * cfg.T]
+    idx, _, _ = route(mine, Wr, b, cfg.G, cfg.M, cfg.K, cfg.gk)
+
+    def host_bias_update(E, T, K, counts, gamma, bias):
+        bias.copy_(torch.from_numpy(bias_update(bias.numpy(), counts.numpy(), T, K, gamma)))
+
+    layer = object.__new__(layer_mod.MoELayer)     # no device buffers: only the end-of-step path
+    layer.cfg = cfg
+    layer.counts = torch.from_numpy(histogram(idx, cfg.E).astype(np.int32))
+    layer.bias = torch.from_numpy(b.copy())
+    real = layer_mod.B.bias_update
+    layer_mod.B.bias_update = host_bias_update
+    try:
+        layer.end_of_step(counts_hook=dp.allreduce_load)
+    finally:
+        layer_mod.B.bias_update = real
+    out[rank] = torch.from_numpy(np.concatenate([layer.counts.numpy().astype(np.float64),
+                                                 layer.bias.numpy().astype(np.float64)]))
+    dist.destroy_process_group()
+
+
+def test_two_rank_layer_end_of_step_matches_single_process():
+    """The layer's own end-of-step path (load all-reduce hook, then the bias
+    update) on two ranks with half a batch each gives the bias of one process
+    that routes the whole batch: the update must judge the summed load against
+    the mean load of all ranks' tokens, not of one rank's."""
+    from oracle.layer import bias_update
+    from oracle.permute import histogram
+    from oracle.route import route
+    from sparse_moe_layer_13_b300 import inputs
+    from sparse_moe_layer_13_b300.configs import MoEConfig
+    world = 2
+    out = torch.zeros(world, 32, dtype=torch.float64).share_memory_()
+    mp.spawn(_layer_step_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+    cfg = MoEConfig("dp", T=64, d=128, E=16, I=128, K=4, G=4, M=2, gk=2, seed=21, bias="uniform")
+    x = inputs.gen_x(cfg).float().numpy()
+    Wr = inputs.gen_router(cfg).numpy()
+    b = inputs.gen_bias(cfg).numpy()
+    idx, _, _ = route(x, Wr, b, cfg.G, cfg.M, cfg.K, cfg.gk)
+    c = histogram(idx, cfg.E)
+    nb = bias_update(b, c, cfg.T, cfg.K, cfg.gamma)
+    # the half-batch mean would flip the sign for experts loaded between the two means
+    assert not np.array_equal(nb, bias_update(b, c, cfg.T // world, cfg.K, cfg.gamma))
+    want = np.concatenate([c.astype(np.float64), nb.astype(np.float64)])
+    for r in range(world):
+        assert np.array_equal(out[r].numpy(), want)
