@@ -151,8 +151,9 @@ def run_ours(args):
 
     K = args.steps
     # GEMM events are external so that, inside a CUDA graph, they become real event records
+    calls = ("route", "permute", "quant", "gemm1", "gemm2", "combine")
     ev = {n: [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-              for _ in range(K)] for n in ("gemm1", "gemm2")}
+              for _ in range(K)] for n in calls}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # one GPU: the K timed steps run as one CUDA graph (13 launches per step, no host work
     # between them); it is replayed once untimed first. Under torchrun the steps run eagerly.
@@ -181,12 +182,13 @@ def run_ours(args):
             dist.barrier()
     binding.check_device_status()
     ms = t0.elapsed_time(t1) / K
-    g1 = statistics.mean(a.elapsed_time(b) for a, b in ev["gemm1"])
-    g2 = statistics.mean(a.elapsed_time(b) for a, b in ev["gemm2"])
+    kt = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in calls}
     if ws > 1:
-        t = torch.tensor([ms, g1, g2], device=dev)
+        t = torch.tensor([ms] + [kt[n] for n in calls], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, g1, g2 = t.tolist()
+        ms, *rest = t.tolist()
+        kt = dict(zip(calls, rest))
+    g1, g2 = kt["gemm1"], kt["gemm2"]
 
     # End to end through the public API: every step copies its x from pinned host
     # memory and its y back to pinned host memory. Copies run on their own streams
@@ -245,6 +247,7 @@ def run_ours(args):
                  "grouped_gemm_tflops": round((f1 + f2) / ((g1 + g2) * 1e-3) / 1e12, 1),
                  "gate_up_gbs": round(g1_gbs, 1)},
         "roofline": roof,
+        "kernels": call_table(cfg, kt, w13_bytes + a_bytes, hbm, bf16, fp8_peak, layer.route_fused),
         "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": cfg.T * cfg.d * 2, "d2h_bytes_per_step": cfg.T * cfg.d * 2},
         "gpu_launches": K * layer.launches_per_forward,
@@ -257,6 +260,52 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def call_table(cfg, kt, gemm1_bytes, hbm, bf16, fp8_peak, fused):
+    """Per-call device time (CUDA events around each call inside the timed step, mean over
+    the K steps), algorithmic bytes and FLOPs, and the fractions of the measured HBM copy
+    bandwidth and tensor peaks they reach. Algorithmic bytes count each input read once and
+    each output written once:
+      route    x T*d*2 + weight planes 3*E*d*2 + choice and gates T*K*8 + summed logits
+               T*E*4 (kept for the backward pass) + the load histogram's read T*K*4;
+               FLOPs 3 * 2*T*d*E (x times the three bf16 terms of Wr, bf16 tensor cores)
+      permute  choice T*K*4 read; grouped row lists (T*K+T)*4 and row_of T*K*4 written
+      quant    x T*d*2 and row_of T*K*4 read; E4M3 rows R*d and scales R*d/128*4 written
+      gemm1    touched W13 and scales, grouped x rows and scales, h and its scales
+      gemm2    FLOPs 2*R*I*d (its bytes are dominated by the same weight stream)
+      combine  routed rows T*K*d*2 (bf16) + shared rows T*d*4 (FP32) + row_of and gates
+               T*K*8 read; y T*d*2 written
+    with R = T*K + T grouped rows."""
+    T, d, E, I, K = cfg.T, cfg.d, cfg.E, cfg.I, cfg.K
+    R = T * K + T
+    f1, f2 = cfg.gemm_flops()
+    work = {
+        "route": (T * d * 2 + 3 * E * d * 2 + T * K * 8 + T * E * 4 + T * K * 4, 6.0 * T * d * E, bf16),
+        "permute": (T * K * 4 + R * 4 + T * K * 4, None, None),
+        "quant": (T * d * 2 + T * K * 4 + R * d + R * (d // 128) * 4, None, None),
+        "gemm1": (gemm1_bytes, f1, fp8_peak),
+        "gemm2": (None, f2, fp8_peak),
+        "combine": (T * K * d * 2 + T * d * 4 + T * K * 8 + T * d * 2, None, None),
+    }
+    out = {}
+    for n, (nbytes, flops, peak) in work.items():
+        ms = kt.get(n)
+        if not ms:
+            continue
+        e = {"ms": round(ms, 4)}
+        if nbytes is not None:
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            e.update(bytes=int(nbytes), gbs=round(gbs, 1), hbm_frac=round(gbs / hbm, 4))
+        if flops is not None:
+            tf = flops / (ms * 1e-3) / 1e12
+            e.update(tflops=round(tf, 1), tensor_frac=round(tf / peak, 4))
+        out[n] = e
+    out["route"]["path"] = "fused" if fused else "k-split"
+    out["route"]["tensor_peak"] = f"bf16 burst {bf16} TFLOP/s (measured)"
+    out["note"] = ("device time per call from CUDA events inside the timed step; hbm_frac of the measured "
+                   f"copy bandwidth {hbm} GB/s, tensor_frac of the measured bf16 burst (route) or 2x it (FP8 GEMMs)")
+    return out
 
 
 TRAIN_METRIC = "MoE layer forward+backward tokens/s; FP8 weight-gradient GEMM TFLOP/s & % of roofline (1 B300)"
@@ -483,7 +532,8 @@ def balancing_loop(cfg, layer, dev, binding, inputs, dp):
     T_all = dp.global_tokens(cfg.T)
     for step in range(cfg.skew_steps):
         x = inputs.gen_x(cfg, dev, step=1000 + step)
-        binding.route(cfg, x, layer.Wr, layer.bias, layer.logit_offset, layer.ws, layer.idx, layer.gate, layer.counts)
+        binding.route_planes(cfg, x, layer.planes, layer.bias, layer.logit_offset, layer.ws, layer.idx, layer.gate,
+                             layer.counts)
         dp.allreduce_load(layer.counts)
         binding.bias_update(cfg.E, T_all, cfg.K, layer.counts, cfg.gamma, layer.bias)
         c = layer.counts.cpu().numpy().astype("float64")
@@ -556,6 +606,38 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_fp8_peak(args):
+    """--fp8-peak: dense E4M3 GEMM throughput of the vendor library on this GPU (torch._scaled_mm,
+    8192^3, per-tensor unit scales, bf16 output), best of 10 timed with CUDA events after 3
+    warm-ups, with the SM clock sampled meanwhile. A measured context figure for the FP8
+    roofline denominators; the reported fractions keep the measured bf16 figure."""
+    import torch
+    torch.cuda.set_device(0)
+    n = 8192
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    a = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn).t()   # column-major operand
+    one = torch.ones((), device="cuda")
+    for _ in range(3):
+        torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    best = float("inf")
+    with ClockSampler(0) as clocks:
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+    tf = 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    _, bf16, _, src = _peaks()
+    print(json.dumps({"measurement": "fp8 e4m3 dense GEMM peak (torch._scaled_mm 8192^3, best of 10)",
+                      "tflops": round(tf, 1), "ms": round(best, 4), "bf16_burst_tflops": bf16,
+                      "ratio_to_bf16": round(tf / bf16, 3), "clocks": clocks.summary()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,7 +653,12 @@ def main():
                     help="pow2: power-of-two 1x128 / 128x128 scales and the block-scaled GEMMs")
     ap.add_argument("--backward", action="store_true",
                     help="time a training step (forward, bias update, backward) instead of the forward")
+    ap.add_argument("--fp8-peak", action="store_true",
+                    help="measure the vendor library's dense E4M3 GEMM rate (8192^3) and exit")
     args = ap.parse_args()
+    if args.fp8_peak:
+        run_fp8_peak(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -116,11 +116,49 @@ size_t moe_workspace_size(const moe_config* cfg);
  *   counts       device i32  [E] out or NULL: pairs routed to each expert
  *   workspace    device, >= moe_workspace_size(cfg) bytes
  * Logits are computed on the tensor cores from x (bf16, exact) times Wr
- * split into three bf16 terms whose sum is Wr exactly, accumulated in FP32. */
+ * split into three bf16 terms whose sum is Wr exactly, accumulated in FP32.
+ * Equivalent to moe_router_planes into the workspace followed by
+ * moe_route_planes(..., MOE_ROUTE_AUTO, ...). The logits stay in the
+ * workspace for moe_route_backward and moe_balance_loss. */
 moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr,
                      const float* logit_offset, const float* bias,
                      int32_t* topk_idx, float* topk_gate, int32_t* counts,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* The router weight as three bf16 planes for moe_route_planes: planes[0] =
+ * bf16(Wr), planes[1] = bf16(Wr - planes[0]), planes[2] = bf16(Wr - planes[0]
+ * - planes[1]), whose sum is Wr exactly (FP32 has 24 significant bits, each
+ * bf16 term 8). A set-up step, to be redone whenever Wr changes.
+ *   Wr      device f32  [E][d]
+ *   planes  device bf16 [3][E][d] out, 16-byte aligned, caller-owned */
+moe_status moe_router_planes(const float* Wr, int32_t E, int32_t d, uint16_t* planes, void* stream);
+
+/* Which router kernels moe_route_planes runs. */
+typedef enum {
+    /* the fused kernel when E <= 256 and ceil(T/128) reaches half the SM
+     * count, otherwise the K-split kernels */
+    MOE_ROUTE_AUTO = 0,
+    /* one kernel, one CTA per 128-token tile: logits accumulated in TMEM in
+     * K splits of at most 24 chunks of 64, the splits summed in registers in
+     * order, the selection run from shared memory; E <= 256 (else
+     * MOE_ERR_UNSUPPORTED_SHAPE) */
+    MOE_ROUTE_FUSED = 1,
+    /* a logits kernel that writes FP32 K-split partials to the workspace,
+     * then a selection kernel that sums them in split order; any E, and the
+     * SMs stay busy for small T */
+    MOE_ROUTE_SPLIT = 2
+} moe_route_path;
+
+/* moe_route with the router weight given as planes (moe_router_planes) and
+ * the kernel path chosen by `path` (moe_route_path; else
+ * MOE_ERR_INVALID_ARG). When both paths use the same number of K splits
+ * (whenever ceil(T/128) * ceil(E/256) alone covers the SMs) they add the
+ * same FP32 partials in the same order and give bit-identical logits,
+ * choices and gates. Other arguments as moe_route; planes 16-byte aligned. */
+moe_status moe_route_planes(const moe_config* cfg, const uint16_t* x, const uint16_t* planes,
+                            const float* logit_offset, const float* bias,
+                            int32_t* topk_idx, float* topk_gate, int32_t* counts, int32_t path,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* Activation quantisation per 1x128 tile ("DeepSeek-V3的MoE架构设计革新" §2
  * item 1; E4M3 largest finite value 448 from "DeepSeek-V3技术解析" §6.2):
@@ -471,6 +509,96 @@ moe_status moe_quant_fp8_128x1_bf16_rows(const uint16_t* x, int64_t x_rows, int6
 moe_status moe_grouped_wgrad_fp8(int32_t groups, const int32_t* offsets, int64_t rows, int64_t width, int32_t M,
                                  int32_t N, const uint8_t* AT, const float* saT, const uint8_t* BT, const float* sbT,
                                  float* out, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Expert parallelism with node-limited routing (《DeepSeek-V3 Technical
+ * Report》深度解读报告 §2.4: a token reaches at most M nodes, chosen by the
+ * sum of their experts' highest affinities; §3.2: tokens cross nodes by
+ * all-to-all, experts spread over the GPUs for prefill).
+ * R ranks; rank r owns the E/R routed experts [r*E/R, (r+1)*E/R) (E % R ==
+ * 0; with R dividing G a rank holds whole groups, so a token reaches at
+ * most M ranks); every rank holds the router and the shared expert and
+ * routes its own T tokens. A step on one rank:
+ *   1. moe_route, moe_quant_fp8_1x128 of its tokens (token order);
+ *   2. moe_ep_dispatch: each token's packed row (E4M3 codes, scales, choice,
+ *      gates; moe_ep_row_bytes) once per destination rank, ordered by
+ *      (rank, token), with per-rank counts (the all-to-all split sizes);
+ *   3. all-to-all of the packed rows (the caller's collective);
+ *   4. moe_ep_receive: the received pairs on this rank's experts, grouped
+ *      by (local expert, received row), codes and scales gathered;
+ *   5. moe_grouped_gemm_fp8 over the E/R local experts (gate/up + SwiGLU,
+ *      then down with MOE_EPI_BF16), weights of experts r*E/R..;
+ *   6. moe_ep_partial: per received row, the gate-weighted sum of its
+ *      local expert outputs (FP32);
+ *   7. the reverse all-to-all of the partial rows (received order);
+ *   8. the shared expert on the rank's own tokens (grouped GEMM with one
+ *      group, FP32 output), then moe_ep_combine.
+ * The pages have no counterpart for these packing formats; the order of
+ * rows is the library's own (stable sorts by rank and by local expert). */
+
+/* Bytes of one packed dispatch row: d code bytes, d/128 FP32 scales, K
+ * expert ids (i32), K gates (f32), zero padding to a multiple of 16. 0 for
+ * d not a multiple of 128 or K outside 1..16. */
+int64_t moe_ep_row_bytes(int32_t d, int32_t K);
+
+/* Workspace bytes of moe_ep_dispatch (rows = cfg->T) and moe_ep_receive
+ * (rows = received rows) for R ranks. 0 for an unsupported cfg or R. */
+size_t moe_ep_workspace_size(const moe_config* cfg, int32_t R, int64_t rows);
+
+/* Send side of the expert-parallel step.
+ *   R            ranks, 1 <= R <= E, E % R == 0 (else MOE_ERR_UNSUPPORTED_SHAPE)
+ *   topk_idx     device i32 [T][K], topk_gate f32 [T][K] (moe_route)
+ *   xq, xs       device u8 [T][d], f32 [T][d/128] (moe_quant_fp8_1x128)
+ *   send_counts  device i32 [R] out or NULL: rows for each rank
+ *   send_offsets device i32 [R+1] out: exclusive prefix of send_counts;
+ *                send_offsets[R] = S, the number of send rows
+ *   send_row_of  device i32 [T][K] out: the send row of the token's first
+ *                slot on each destination rank, -1 for later slots on the
+ *                same rank
+ *   send_token   device i32 [T*min(K,R)] out: token of each send row
+ *   send_buf     device u8 [T*min(K,R)][moe_ep_row_bytes(d,K)] out: rows
+ *                [0, S) written, ordered by (rank, token)
+ *   workspace    device, >= moe_ep_workspace_size(cfg, R, T) bytes
+ * Expert ids outside [0, E) set MOE_ERR_DEVICE_CHECK and are skipped. */
+moe_status moe_ep_dispatch(const moe_config* cfg, int32_t R, const int32_t* topk_idx, const float* topk_gate,
+                           const uint8_t* xq, const float* xs, int32_t* send_counts, int32_t* send_offsets,
+                           int32_t* send_row_of, int32_t* send_token, uint8_t* send_buf,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Receive side: groups the received rows' pairs on this rank's experts.
+ *   rank          0 <= rank < R; its experts are [rank*E/R, (rank+1)*E/R)
+ *   n_recv        received packed rows (any order of source ranks)
+ *   recv_buf      device u8 [n_recv][moe_ep_row_bytes(d,K)]
+ *   local_offsets device i32 [E/R + 1] out: grouped rows of each local
+ *                 expert; local_offsets[E/R] = P, the pairs this rank serves
+ *   local_counts  device i32 [E/R] out or NULL
+ *   sorted_row    device i32 [n_recv*K] out: received row of grouped row p < P
+ *   row_of        device i32 [n_recv][K] out: grouped row of each (row, slot)
+ *                 on this rank, -1 for slots served elsewhere
+ *   xq_local      device u8 [n_recv*K][d] out, xs_local f32 [n_recv*K][d/128]
+ *                 out: rows [0, P) in grouped order
+ *   workspace     device, >= moe_ep_workspace_size(cfg, R, n_recv) bytes */
+moe_status moe_ep_receive(const moe_config* cfg, int32_t R, int32_t rank, int64_t n_recv, const uint8_t* recv_buf,
+                          int32_t* local_offsets, int32_t* local_counts, int32_t* sorted_row, int32_t* row_of,
+                          uint8_t* xq_local, float* xs_local, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Per received row i: partial[i] = sum over slots k with row_of[i][k] >= 0,
+ * in slot order, of gate[i][k] * routed_out[row_of[i][k]] (FP32 accumulation).
+ *   routed_out device bf16 [out_rows][d] (the down GEMM's grouped rows;
+ *              row_of values >= out_rows set MOE_ERR_DEVICE_CHECK)
+ *   partial    device f32 [n_recv][d] out */
+moe_status moe_ep_partial(const moe_config* cfg, int64_t n_recv, const uint8_t* recv_buf, const int32_t* row_of,
+                          const uint16_t* routed_out, int64_t out_rows, float* partial, void* stream);
+
+/* y[t] = shared_out[t] + sum over the token's send rows (send_row_of[t][k]
+ * >= 0, slot order) of returned[row] (+ residual[t]), FP32 accumulation,
+ * bf16 result.
+ *   shared_out device f32 [T][d]; returned device f32 [S][d], the partial
+ *   rows back from the ranks, in send order; residual bf16 [T][d] or NULL;
+ *   y device bf16 [T][d] out */
+moe_status moe_ep_combine(const moe_config* cfg, const float* shared_out, const float* returned, int64_t S,
+                          const int32_t* send_row_of, const uint16_t* residual, uint16_t* y, void* stream);
 
 /* Failure-detection self test: launches one kernel that waits, with a
  * limit of `limit_us` microseconds, on a barrier nothing will complete, and

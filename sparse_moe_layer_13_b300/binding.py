@@ -38,6 +38,8 @@ _SIG = {
     "moe_check_device_status": (ctypes.c_int, [_P]),
     "moe_workspace_size": (ctypes.c_size_t, [_P]),
     "moe_route": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_router_planes": (ctypes.c_int, [_P, _I32, _I32, _P, _P]),
+    "moe_route_planes": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, ctypes.c_size_t, _P]),
     "moe_quant_fp8_1x128": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P]),
     "moe_quant_fp8_128x128": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P]),
     "moe_pack_w13": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
@@ -66,6 +68,12 @@ _SIG = {
     "moe_quant_fp8_128x1_bf16_rows": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _I32, _P, _I64, _I32, _I32, _P, _I64, _P,
                                                      _P]),
     "moe_grouped_wgrad_fp8": (ctypes.c_int, [_I32, _P, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]),
+    "moe_ep_row_bytes": (ctypes.c_int64, [_I32, _I32]),
+    "moe_ep_workspace_size": (ctypes.c_size_t, [_P, _I32, _I64]),
+    "moe_ep_dispatch": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_ep_receive": (ctypes.c_int, [_P, _I32, _I32, _I64, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_ep_partial": (ctypes.c_int, [_P, _I64, _P, _P, _P, _I64, _P, _P]),
+    "moe_ep_combine": (ctypes.c_int, [_P, _P, _P, _I64, _P, _P, _P, _P]),
 }
 
 
@@ -167,6 +175,41 @@ def route(cfg, x, Wr, bias, logit_offset=None, workspace=None, idx=None, gate=No
     c = config_c(cfg)
     _call("moe_route", ctypes.byref(c), _ptr(x), _ptr(Wr), _ptr(logit_offset), _ptr(bias), _ptr(idx), _ptr(gate),
           _ptr(counts), _ptr(workspace), workspace.numel(), _stream())
+    return idx, gate, counts
+
+
+ROUTE_PATHS = {"auto": 0, "fused": 1, "split": 2}
+
+
+def router_planes(Wr, planes=None):
+    """Wr f32 [E][d] -> the three bf16 planes [3][E][d] (moe_router_planes)."""
+    _need(Wr, torch.float32, "Wr")
+    E, d = Wr.shape
+    planes = torch.empty(3, E, d, dtype=torch.bfloat16, device=Wr.device) if planes is None else planes
+    _need(planes, torch.bfloat16, "planes", (3, E, d))
+    _call("moe_router_planes", _ptr(Wr), E, d, _ptr(planes), _stream())
+    return planes
+
+
+def route_planes(cfg, x, planes, bias, logit_offset=None, workspace=None, idx=None, gate=None, counts=None,
+                 want_counts=False, path="auto"):
+    """moe_route_planes: the router on pre-split weight planes, on the kernel path `path`
+    ("auto", "fused" or "split")."""
+    dev = x.device
+    _need(x, torch.bfloat16, "x", (cfg.T, cfg.d))
+    _need(planes, torch.bfloat16, "planes", (3, cfg.E, cfg.d))
+    _need(bias, torch.float32, "bias", (cfg.E,))
+    if logit_offset is not None:
+        _need(logit_offset, torch.float32, "logit_offset", (cfg.E,))
+    idx = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev) if idx is None else idx
+    gate = torch.empty(cfg.T, cfg.K, dtype=torch.float32, device=dev) if gate is None else gate
+    if want_counts and counts is None:
+        counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_size(cfg), dtype=torch.uint8, device=dev)
+    c = config_c(cfg)
+    _call("moe_route_planes", ctypes.byref(c), _ptr(x), _ptr(planes), _ptr(logit_offset), _ptr(bias), _ptr(idx),
+          _ptr(gate), _ptr(counts), ROUTE_PATHS[path], _ptr(workspace), workspace.numel(), _stream())
     return idx, gate, counts
 
 
@@ -505,3 +548,83 @@ def grouped_wgrad_fp8(offsets, rows, AT, saT, BT, sbT, out=None):
     _call("moe_grouped_wgrad_fp8", groups, _ptr(offsets), rows, width, M, N, _ptr(AT), _ptr(saT), _ptr(BT), _ptr(sbT),
           _ptr(out), _stream())
     return out
+
+
+# ------------------------------------------------------------------ expert parallel ----
+def ep_row_bytes(d: int, K: int) -> int:
+    return int(load().moe_ep_row_bytes(d, K))
+
+
+def ep_workspace_size(cfg, R: int, rows: int) -> int:
+    c = config_c(cfg)
+    return int(load().moe_ep_workspace_size(ctypes.byref(c), R, rows))
+
+
+def ep_dispatch(cfg, R, idx, gate, xq, xs, workspace=None):
+    """moe_ep_dispatch: packed send rows ordered by (destination rank, token). Returns a dict
+    with send_counts [R], send_offsets [R+1], send_row_of [T][K], send_token and send_buf
+    (capacity T*min(K,R) rows; the first send_offsets[R] are written)."""
+    dev = idx.device
+    _need(idx, torch.int32, "topk_idx", (cfg.T, cfg.K))
+    _need(gate, torch.float32, "topk_gate", (cfg.T, cfg.K))
+    _need(xq, torch.uint8, "xq", (cfg.T, cfg.d))
+    _need(xs, torch.float32, "xs", (cfg.T, cfg.d // 128))
+    cap = cfg.T * min(cfg.K, R)
+    out = {"send_counts": torch.empty(R, dtype=torch.int32, device=dev),
+           "send_offsets": torch.empty(R + 1, dtype=torch.int32, device=dev),
+           "send_row_of": torch.empty(cfg.T, cfg.K, dtype=torch.int32, device=dev),
+           "send_token": torch.empty(cap, dtype=torch.int32, device=dev),
+           "send_buf": torch.empty(cap, ep_row_bytes(cfg.d, cfg.K), dtype=torch.uint8, device=dev)}
+    if workspace is None:
+        workspace = torch.empty(max(ep_workspace_size(cfg, R, cfg.T), 16), dtype=torch.uint8, device=dev)
+    c = config_c(cfg)
+    _call("moe_ep_dispatch", ctypes.byref(c), R, _ptr(idx), _ptr(gate), _ptr(xq), _ptr(xs), _ptr(out["send_counts"]),
+          _ptr(out["send_offsets"]), _ptr(out["send_row_of"]), _ptr(out["send_token"]), _ptr(out["send_buf"]),
+          _ptr(workspace), workspace.numel(), _stream())
+    return out
+
+
+def ep_receive(cfg, R, rank, recv_buf, workspace=None, want_counts=False):
+    """moe_ep_receive on packed rows recv_buf u8 [n][row_bytes]: this rank's pairs grouped by
+    local expert, with their codes and scales gathered (capacity n*K rows)."""
+    n = recv_buf.shape[0]
+    dev = recv_buf.device
+    _need(recv_buf, torch.uint8, "recv_buf", (n, ep_row_bytes(cfg.d, cfg.K)))
+    nl = cfg.E // R
+    cap = max(n * cfg.K, 1)
+    out = {"local_offsets": torch.empty(nl + 1, dtype=torch.int32, device=dev),
+           "local_counts": torch.empty(nl, dtype=torch.int32, device=dev) if want_counts else None,
+           "sorted_row": torch.empty(cap, dtype=torch.int32, device=dev),
+           "row_of": torch.empty(max(n, 1), cfg.K, dtype=torch.int32, device=dev),
+           "xq_local": torch.empty(cap, cfg.d, dtype=torch.uint8, device=dev),
+           "xs_local": torch.empty(cap, cfg.d // 128, dtype=torch.float32, device=dev)}
+    if workspace is None:
+        workspace = torch.empty(max(ep_workspace_size(cfg, R, n), 16), dtype=torch.uint8, device=dev)
+    c = config_c(cfg)
+    _call("moe_ep_receive", ctypes.byref(c), R, rank, n, _ptr(recv_buf) if n else None, _ptr(out["local_offsets"]),
+          _ptr(out["local_counts"]), _ptr(out["sorted_row"]), _ptr(out["row_of"]), _ptr(out["xq_local"]),
+          _ptr(out["xs_local"]), _ptr(workspace), workspace.numel(), _stream())
+    return out
+
+
+def ep_partial(cfg, recv_buf, row_of, routed_out, partial=None):
+    """moe_ep_partial: per received row the gate-weighted sum of this rank's expert outputs (FP32)."""
+    n = recv_buf.shape[0]
+    _need(routed_out, torch.bfloat16, "routed_out")
+    partial = torch.empty(n, cfg.d, dtype=torch.float32, device=recv_buf.device) if partial is None else partial
+    c = config_c(cfg)
+    _call("moe_ep_partial", ctypes.byref(c), n, _ptr(recv_buf), _ptr(row_of), _ptr(routed_out), routed_out.shape[0],
+          _ptr(partial), _stream())
+    return partial
+
+
+def ep_combine(cfg, shared_out, returned, send_row_of, residual=None, y=None):
+    """moe_ep_combine: y = shared + the partial rows returned for each token (+ residual), bf16."""
+    _need(shared_out, torch.float32, "shared_out", (cfg.T, cfg.d))
+    _need(send_row_of, torch.int32, "send_row_of", (cfg.T, cfg.K))
+    _need(returned, torch.float32, "returned")
+    y = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16, device=shared_out.device) if y is None else y
+    c = config_c(cfg)
+    _call("moe_ep_combine", ctypes.byref(c), _ptr(shared_out), _ptr(returned) if returned.numel() else None,
+          returned.shape[0], _ptr(send_row_of), _ptr(residual), _ptr(y), _stream())
+    return y

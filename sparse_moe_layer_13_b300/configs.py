@@ -33,6 +33,7 @@ class MoEConfig:
     gamma: float = 1e-3             # bias update speed
     zipf_s: Optional[float] = None  # per-expert router logit offsets when set
     zipf_c: float = 0.0             # scale of those offsets
+    expert_seed: Optional[int] = None  # seed of the expert weights (default: seed)
 
     @property
     def rows(self) -> int:
@@ -52,6 +53,10 @@ class MoEConfig:
         rows = self.rows
         return 4.0 * rows * self.d * self.I, 2.0 * rows * self.I * self.d
 
+    @property
+    def weight_seed(self) -> int:
+        return self.seed if self.expert_seed is None else self.expert_seed
+
     def abi(self) -> tuple[int, ...]:
         return (self.T, self.d, self.E, self.I, self.K, self.G, self.M, self.gk)
 
@@ -61,12 +66,14 @@ class MoEConfig:
 
 TINY = MoEConfig("tiny", T=256, d=256, E=16, I=128, K=4, G=4, M=2, gk=2, seed=0, bias="uniform")
 MID = MoEConfig("mid", T=4096, d=2048, E=64, I=1408, K=6, G=8, M=3, gk=2, seed=1)
+# The three full-width workloads run the same layer: one set of expert weights
+# (seed 2) on different batches, routers and biases (their own seeds).
 FULL = MoEConfig("full", T=16384, d=7168, E=256, I=2048, K=8, G=8, M=4, gk=2, seed=2)
-DECODE = MoEConfig("decode", T=128, d=7168, E=256, I=2048, K=8, G=8, M=4, gk=2, seed=3)
+DECODE = MoEConfig("decode", T=128, d=7168, E=256, I=2048, K=8, G=8, M=4, gk=2, seed=3, expert_seed=2)
 # c = 0.274886: bisection with the FP64 reference router on a seeded 8192-token
 # batch for a hottest-expert load of 8x the mean at step 0 (tests/golden/calibrate_skew.py)
 SKEW = MoEConfig("skew", T=65536, d=7168, E=256, I=2048, K=8, G=8, M=4, gk=2, seed=4,
-                 skew_steps=50, gamma=1e-3, zipf_s=1.1, zipf_c=0.274886)
+                 skew_steps=50, gamma=1e-3, zipf_s=1.1, zipf_c=0.274886, expert_seed=2)
 
 CONFIGS = {c.name: c for c in (TINY, MID, FULL, DECODE, SKEW)}
 

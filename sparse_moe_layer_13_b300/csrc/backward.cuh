@@ -142,12 +142,15 @@ combine_backward_kernel(const uint16_t* __restrict__ dy, const uint16_t* __restr
 }
 
 // One warp per token; lane k < K holds chosen expert k. The affinity is
-// recomputed from the router's K-split logits with the selection's own
-// arithmetic, so s and S are the values the gates were made from.
+// recomputed from the router's stored logits (K-split partials or their sums,
+// as the workspace word `splits` says) with the selection's own arithmetic,
+// so s and S are the values the gates were made from.
 __global__ void __launch_bounds__(128)
-route_backward_kernel(const float* __restrict__ z, int ksplit, int T, int E, int K, const float* __restrict__ offset,
-                      const int32_t* __restrict__ topk_idx, const float* __restrict__ dgate, float* __restrict__ dz) {
+route_backward_kernel(const float* __restrict__ z, const int* __restrict__ splits, int T, int E, int K,
+                      const float* __restrict__ offset, const int32_t* __restrict__ topk_idx,
+                      const float* __restrict__ dgate, float* __restrict__ dz) {
     const int lane = static_cast<int>(lane_id());
+    const int ksplit = *splits;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
     const int64_t TE = static_cast<int64_t>(T) * E;

@@ -8,6 +8,7 @@
 
 #include "backward.cuh"
 #include "common.cuh"
+#include "ep.cuh"
 #include "gemm_fp8.cuh"
 #include "gemm_wgrad.cuh"
 #include "gemm_mx.cuh"
@@ -84,18 +85,39 @@ int route_ksplit(const moe_config* c) {
     return (nchunks + per - 1) / per;
 }
 
-// Workspace layout: [router logit partials f32 ksplit*T*E][router weight
-// planes bf16 3*E*d][per-block counts i32 nblk*E][per-block bases i32
-// nblk*E][offsets scratch i32 E+2][balance chunk sums f32, i32 (T/32)*E each]
+// K split of the fused router: the accumulation bound alone (each split at
+// most rtc::kMaxChunksPerSplit chunks), normalised so that every split gets
+// at least one chunk. Equal to route_ksplit whenever the batch alone fills
+// the SMs, so the two paths then add the same partials in the same order.
+int route_ksplit_acc(const moe_config* c) {
+    const int nchunks = 3 * (c->d / rtc::BK);
+    const int ks = (nchunks + rtc::kMaxChunksPerSplit - 1) / rtc::kMaxChunksPerSplit;
+    const int per = (nchunks + ks - 1) / ks;
+    return (nchunks + per - 1) / per;
+}
+
+// The fused router serves E <= 256 when its one CTA per 128-token tile covers
+// at least half the SMs; smaller batches take the K-split path, whose extra
+// CTAs fill the GPU.
+bool route_fused_auto(const moe_config* c) {
+    return c->E <= rtc::BN_MAX && 2 * ceil_div(c->T, rtc::BM) >= num_sms();
+}
+
+// Workspace layout: [header: split count of the stored router logits, i32,
+// written by the router kernels][router logit partials f32 ksplit*T*E (the
+// fused router stores their sums in the first T*E)][router weight planes bf16
+// 3*E*d][per-block counts i32 nblk*E][per-block bases i32 nblk*E][offsets
+// scratch i32 E+2][balance chunk sums f32, i32 (T/32)*E each]
 struct WsLayout {
-    size_t logits, planes, blk_counts, blk_base, offsets, balance, total;
+    size_t header, logits, planes, blk_counts, blk_base, offsets, balance, total;
 };
 
 WsLayout ws_layout(const moe_config* c) {
     WsLayout w{};
     const int64_t nblk = ceil_div(c->T, perm::kTokPerBlk);
-    w.logits = 0;
-    w.planes = align_up(static_cast<size_t>(route_ksplit(c)) * c->T * c->E * sizeof(float), 256);
+    w.header = 0;
+    w.logits = 256;
+    w.planes = w.logits + align_up(static_cast<size_t>(route_ksplit(c)) * c->T * c->E * sizeof(float), 256);
     w.blk_counts = w.planes + align_up(static_cast<size_t>(3) * c->E * c->d * sizeof(uint16_t), 256);
     w.blk_base = w.blk_counts + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
     w.offsets = w.blk_base + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
@@ -187,6 +209,39 @@ void launch_select(const moe_config* c, const float* z, int ks, const float* off
     else if (epl <= 8) launch_select_e<8>(c, z, ks, off, bias, idx, gate, grid, smem, st);
     else if (epl <= 16) launch_select_e<16>(c, z, ks, off, bias, idx, gate, grid, smem, st);
     else launch_select_e<32>(c, z, ks, off, bias, idx, gate, grid, smem, st);
+}
+
+template <int EPL, int MAXGK>
+moe_status launch_fused_t(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, int ks,
+                          const float* off, const float* bias, int32_t* idx, float* gate, float* z, int* splits,
+                          cudaStream_t st) {
+    static std::atomic<uint64_t> attr_done{0};
+    if (smem_attr(reinterpret_cast<const void*>(rtc::fused_kernel<EPL, MAXGK>), rtc::F_SMEM_BYTES, attr_done) !=
+        MOE_OK)
+        return MOE_ERR_CUDA;
+    rtc::FParams fp{c->T, c->d, c->E, ks, c->G, c->M, c->K, c->gk, off, bias, idx, gate, z, splits};
+    rtc::fused_kernel<EPL, MAXGK><<<static_cast<unsigned>(ceil_div(c->T, rtc::BM)), rtc::F_THREADS,
+                                    rtc::F_SMEM_BYTES, st>>>(tx, tw, fp);
+    return launch_status();
+}
+
+template <int EPL>
+moe_status launch_fused_e(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, int ks,
+                          const float* off, const float* bias, int32_t* idx, float* gate, float* z, int* splits,
+                          cudaStream_t st) {
+    if (c->gk <= 2) return launch_fused_t<EPL, 2>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
+    if (c->gk <= 4) return launch_fused_t<EPL, 4>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
+    return launch_fused_t<EPL, route::kMaxGK>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
+}
+
+// The fused router (E <= 256: at most 8 experts per lane).
+moe_status launch_fused(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, int ks, const float* off,
+                        const float* bias, int32_t* idx, float* gate, float* z, int* splits, cudaStream_t st) {
+    const int epl = (c->E + 31) / 32;
+    if (epl <= 1) return launch_fused_e<1>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
+    if (epl <= 2) return launch_fused_e<2>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
+    if (epl <= 4) return launch_fused_e<4>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
+    return launch_fused_e<8>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
 }
 
 // to: the FP32 output's tensor map for the all-FP32 epilogues (unused by the others)
@@ -315,11 +370,12 @@ moe_status permute_scratch(int32_t** out) {
 }
 
 template <int EPL>
-void launch_balance_partial(const float* z, int ks, const moe_config* c, const float* offset, const int32_t* idx,
-                            float* p_part, int32_t* c_part, cudaStream_t st) {
+void launch_balance_partial(const float* z, const int* splits, const moe_config* c, const float* offset,
+                            const int32_t* idx, float* p_part, int32_t* c_part, cudaStream_t st) {
     const int nchunk = c->T / 32;
     const int grid = static_cast<int>(std::min<int64_t>(ceil_div(nchunk, 4), static_cast<int64_t>(num_sms()) * 8));
-    route::balance_partial_kernel<EPL><<<grid, 128, 0, st>>>(z, ks, c->T, c->E, c->K, offset, idx, p_part, c_part);
+    route::balance_partial_kernel<EPL><<<grid, 128, 0, st>>>(z, splits, c->T, c->E, c->K, offset, idx, p_part,
+                                                             c_part);
 }
 
 // Checks shared by the 128x1 grouped quantisers; returns MOE_OK to launch.
@@ -377,54 +433,84 @@ size_t moe_workspace_size(const moe_config* cfg) {
     return ws_layout(cfg).total;
 }
 
-moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr, const float* logit_offset,
-                     const float* bias, int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+moe_status moe_router_planes(const float* Wr, int32_t E, int32_t d, uint16_t* planes, void* stream) {
+    if (!Wr || !planes || E < 1 || d < 1) return MOE_ERR_INVALID_ARG;
+    const int64_t nw = static_cast<int64_t>(E) * d;
+    rtc::split_kernel<<<static_cast<unsigned>(ceil_div(nw, 256)), 256, 0, as_stream(stream)>>>(Wr, nw, planes);
+    return launch_status();
+}
+
+moe_status moe_route_planes(const moe_config* cfg, const uint16_t* x, const uint16_t* planes,
+                            const float* logit_offset, const float* bias, int32_t* topk_idx, float* topk_gate,
+                            int32_t* counts, int32_t path, void* workspace, size_t workspace_bytes, void* stream) {
     const moe_status cs = check_config(cfg);
     if (cs != MOE_OK) return cs;
-    if (!x || !Wr || !bias || !topk_idx || !topk_gate) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(Wr) || !aligned16(topk_idx) || !aligned16(topk_gate)) return MOE_ERR_INVALID_ARG;
+    if (!x || !planes || !bias || !topk_idx || !topk_gate) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(planes) || !aligned16(topk_idx) || !aligned16(topk_gate))
+        return MOE_ERR_INVALID_ARG;
+    if (path != MOE_ROUTE_AUTO && path != MOE_ROUTE_FUSED && path != MOE_ROUTE_SPLIT) return MOE_ERR_INVALID_ARG;
+    if (path == MOE_ROUTE_FUSED && cfg->E > rtc::BN_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
     const WsLayout wl = ws_layout(cfg);
     if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    const bool fused = path == MOE_ROUTE_FUSED || (path == MOE_ROUTE_AUTO && route_fused_auto(cfg));
     cudaStream_t st = as_stream(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* splits = reinterpret_cast<int*>(ws + wl.header);
     float* z = reinterpret_cast<float*>(ws + wl.logits);
-    uint16_t* planes = reinterpret_cast<uint16_t*>(ws + wl.planes);
-    const int64_t nw = static_cast<int64_t>(cfg->E) * cfg->d;
-    rtc::split_kernel<<<static_cast<unsigned>(ceil_div(nw, 256)), 256, 0, st>>>(Wr, nw, planes);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    const int ks = route_ksplit(cfg);
     const int bn = std::min(cfg->E, rtc::BN_MAX);
     CUtensorMap tx, tw;
     if (!make_map_bf16(&tx, x, static_cast<uint64_t>(cfg->d), static_cast<uint64_t>(cfg->T), rtc::BM)) return MOE_ERR_CUDA;
     if (!make_map_bf16(&tw, planes, static_cast<uint64_t>(cfg->d), static_cast<uint64_t>(3) * cfg->E,
                        static_cast<uint32_t>(bn)))
         return MOE_ERR_CUDA;
-    static std::atomic<uint64_t> attr_done{0};
-    if (smem_attr(reinterpret_cast<const void*>(rtc::logits_kernel), rtc::SMEM_BYTES, attr_done) != MOE_OK)
-        return MOE_ERR_CUDA;
-    const dim3 lg(static_cast<unsigned>(ceil_div(cfg->T, rtc::BM)), static_cast<unsigned>(ceil_div(cfg->E, rtc::BN_MAX)),
-                  static_cast<unsigned>(ks));
-    rtc::Params rp{cfg->T, cfg->d, cfg->E, bn, ks, z};
-    rtc::logits_kernel<<<lg, rtc::NUM_THREADS, rtc::SMEM_BYTES, st>>>(tx, tw, rp);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    const size_t sel_smem = static_cast<size_t>(route::kSelWarps) * 2 * cfg->E * sizeof(float);
-    const int sel_grid = static_cast<int>(std::min<int64_t>(ceil_div(cfg->T, route::kSelWarps), 65535));
-    launch_select(cfg, z, ks, logit_offset, bias, topk_idx, topk_gate, sel_grid, sel_smem, st);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (fused) {
+        if (launch_fused(cfg, tx, tw, route_ksplit_acc(cfg), logit_offset, bias, topk_idx, topk_gate, z, splits, st) !=
+            MOE_OK)
+            return MOE_ERR_CUDA;
+    } else {
+        const int ks = route_ksplit(cfg);
+        static std::atomic<uint64_t> attr_done{0};
+        if (smem_attr(reinterpret_cast<const void*>(rtc::logits_kernel), rtc::SMEM_BYTES, attr_done) != MOE_OK)
+            return MOE_ERR_CUDA;
+        const dim3 lg(static_cast<unsigned>(ceil_div(cfg->T, rtc::BM)),
+                      static_cast<unsigned>(ceil_div(cfg->E, rtc::BN_MAX)), static_cast<unsigned>(ks));
+        rtc::Params rp{cfg->T, cfg->d, cfg->E, bn, ks, z, splits};
+        rtc::logits_kernel<<<lg, rtc::NUM_THREADS, rtc::SMEM_BYTES, st>>>(tx, tw, rp);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+        const size_t sel_smem = static_cast<size_t>(route::kSelWarps) * 2 * cfg->E * sizeof(float);
+        const int sel_grid = static_cast<int>(std::min<int64_t>(ceil_div(cfg->T, route::kSelWarps), 65535));
+        launch_select(cfg, z, ks, logit_offset, bias, topk_idx, topk_gate, sel_grid, sel_smem, st);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
     if (counts != nullptr) {
         const int nblk = static_cast<int>(ceil_div(cfg->T, perm::kTokPerBlk));
         int32_t* blk_counts = reinterpret_cast<int32_t*>(ws + wl.blk_counts);
         int32_t* blk_base = reinterpret_cast<int32_t*>(ws + wl.blk_base);
         const size_t hsm = static_cast<size_t>(perm::kWarps) * cfg->E * sizeof(int);
         const int64_t npairs = static_cast<int64_t>(cfg->T) * cfg->K;
-        perm::hist_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E, blk_counts);
+        perm::hist_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(perm::KeyExpert{topk_idx, cfg->E}, npairs, cfg->K,
+                                                                 cfg->E, blk_counts);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
         int32_t* offs = reinterpret_cast<int32_t*>(ws + wl.offsets);
         perm::scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, cfg->E, cfg->T, cfg->K, blk_base, offs, counts);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, const uint16_t* x, const float* Wr, const float* logit_offset,
+                     const float* bias, int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    const moe_status cs = check_config(cfg);
+    if (cs != MOE_OK) return cs;
+    if (!Wr || !aligned16(Wr)) return MOE_ERR_INVALID_ARG;
+    const WsLayout wl = ws_layout(cfg);
+    if (workspace == nullptr || workspace_bytes < wl.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    uint16_t* planes = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + wl.planes);
+    const moe_status ps = moe_router_planes(Wr, cfg->E, cfg->d, planes, stream);
+    if (ps != MOE_OK) return ps;
+    return moe_route_planes(cfg, x, planes, logit_offset, bias, topk_idx, topk_gate, counts, MOE_ROUTE_AUTO,
+                            workspace, workspace_bytes, stream);
 }
 
 moe_status moe_quant_fp8_1x128_rule(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int32_t rule,
@@ -525,12 +611,13 @@ moe_status moe_permute(const moe_config* cfg, const int32_t* topk_idx, const uin
     const int nblk = static_cast<int>(ceil_div(cfg->T, perm::kTokPerBlk));
     const int64_t npairs = static_cast<int64_t>(cfg->T) * cfg->K;
     const size_t hsm = static_cast<size_t>(perm::kWarps) * cfg->E * sizeof(int);
-    perm::hist_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E, blk_counts);
+    perm::hist_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(perm::KeyExpert{topk_idx, cfg->E}, npairs, cfg->K,
+                                                                 cfg->E, blk_counts);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     perm::scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, cfg->E, cfg->T, cfg->K, blk_base, offsets, counts);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    perm::scatter_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E, blk_base, row_of,
-                                                               sorted_token);
+    perm::scatter_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(perm::KeyExpert{topk_idx, cfg->E}, npairs, cfg->K,
+                                                               cfg->E, blk_base, row_of, sorted_token);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     if (!gather_rows) return MOE_OK;
     const int64_t rows = npairs + cfg->T;
@@ -549,18 +636,18 @@ moe_status moe_balance_loss(const moe_config* cfg, const float* logit_offset, co
     if (workspace_bytes < w.total) return MOE_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const float* z = reinterpret_cast<const float*>(ws + w.logits);
+    const int* splits = reinterpret_cast<const int*>(ws + w.header);
     float* p_part = reinterpret_cast<float*>(ws + w.balance);
     int32_t* c_part = reinterpret_cast<int32_t*>(
         ws + w.balance + align_up(static_cast<size_t>(ceil_div(cfg->T, 32)) * cfg->E * sizeof(float), 256));
-    const int ks = route_ksplit(cfg);
     const cudaStream_t st = as_stream(stream);
     const int epl = (cfg->E + 31) / 32;
     if (epl <= 8)
-        launch_balance_partial<8>(z, ks, cfg, logit_offset, topk_idx, p_part, c_part, st);
+        launch_balance_partial<8>(z, splits, cfg, logit_offset, topk_idx, p_part, c_part, st);
     else if (epl <= 16)
-        launch_balance_partial<16>(z, ks, cfg, logit_offset, topk_idx, p_part, c_part, st);
+        launch_balance_partial<16>(z, splits, cfg, logit_offset, topk_idx, p_part, c_part, st);
     else
-        launch_balance_partial<32>(z, ks, cfg, logit_offset, topk_idx, p_part, c_part, st);
+        launch_balance_partial<32>(z, splits, cfg, logit_offset, topk_idx, p_part, c_part, st);
     const int nseq = cfg->T / seq_len;
     route::balance_final_kernel<<<ceil_div(nseq, 4), 128, 0, st>>>(p_part, c_part, nseq, seq_len, cfg->E, cfg->K,
                                                                    alpha, f, P, loss);
@@ -588,14 +675,14 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx, c
     cudaStream_t st = as_stream(stream);
     const int64_t npairs = static_cast<int64_t>(cfg->T) * cfg->K;
     const size_t hsm = static_cast<size_t>(perm::kWarps) * cfg->E * sizeof(int);
-    perm::hist_kernel<<<static_cast<unsigned>(nblk), perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E,
-                                                                                   blk_counts);
+    perm::hist_kernel<<<static_cast<unsigned>(nblk), perm::kWarps * 32, hsm, st>>>(
+        perm::KeyExpert{topk_idx, cfg->E}, npairs, cfg->K, cfg->E, blk_counts);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     perm::scan_kernel<<<1, 1024, 0, st>>>(blk_counts, static_cast<int>(nblk), cfg->E, cfg->T, cfg->K, blk_base,
                                           offsets, counts);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    perm::scatter_kernel<<<static_cast<unsigned>(nblk), perm::kWarps * 32, hsm, st>>>(topk_idx, npairs, cfg->K, cfg->E,
-                                                                                      blk_base, row_of, sorted_token);
+    perm::scatter_kernel<<<static_cast<unsigned>(nblk), perm::kWarps * 32, hsm, st>>>(
+        perm::KeyExpert{topk_idx, cfg->E}, npairs, cfg->K, cfg->E, blk_base, row_of, sorted_token);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     if (!gather_rows) return MOE_OK;
     const int64_t rows = npairs + cfg->T;
@@ -686,9 +773,11 @@ moe_status moe_route_backward(const moe_config* cfg, const float* logit_offset, 
     if (!topk_idx || !dgate || !dz) return MOE_ERR_INVALID_ARG;
     const WsLayout wl = ws_layout(cfg);
     if (workspace == nullptr || workspace_bytes < wl.total) return MOE_ERR_WORKSPACE;
-    const float* z = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) + wl.logits);
+    const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+    const float* z = reinterpret_cast<const float*>(ws + wl.logits);
+    const int* splits = reinterpret_cast<const int*>(ws + wl.header);
     bwd::route_backward_kernel<<<static_cast<unsigned>(ceil_div(cfg->T, 4)), 128, 0, as_stream(stream)>>>(
-        z, route_ksplit(cfg), cfg->T, cfg->E, cfg->K, logit_offset, topk_idx, dgate, dz);
+        z, splits, cfg->T, cfg->E, cfg->K, logit_offset, topk_idx, dgate, dz);
     return launch_status();
 }
 
@@ -800,6 +889,112 @@ moe_status moe_grouped_wgrad_fp8(int32_t groups, const int32_t* offsets, int64_t
     const int64_t tiles = static_cast<int64_t>(groups) * (M / gemm::BM) * (N / gemm::BN);
     const int grid = static_cast<int>(std::min<int64_t>(num_sms(), tiles));
     wgrad::grouped_wgrad_fp8_kernel<<<grid, gemm::NUM_THREADS, wgrad::SMEM_BYTES, as_stream(stream)>>>(ta, tb, to, p);
+    return launch_status();
+}
+
+// ------------------------------------------------------ expert parallel ----
+int64_t moe_ep_row_bytes(int32_t d, int32_t K) {
+    if (d < 128 || d % 128 || K < 1 || K > 16) return 0;
+    return ep::row_bytes(d, K);
+}
+
+size_t moe_ep_workspace_size(const moe_config* cfg, int32_t R, int64_t rows) {
+    if (check_config(cfg) != MOE_OK || R < 1 || R > cfg->E || cfg->E % R || rows < 0) return 0;
+    const int64_t keys = std::max<int64_t>(R, cfg->E / R);
+    return 2 * align_up(static_cast<size_t>(ceil_div(std::max<int64_t>(rows, 1), perm::kTokPerBlk)) * keys * 4, 256);
+}
+
+moe_status moe_ep_dispatch(const moe_config* cfg, int32_t R, const int32_t* topk_idx, const float* topk_gate,
+                           const uint8_t* xq, const float* xs, int32_t* send_counts, int32_t* send_offsets,
+                           int32_t* send_row_of, int32_t* send_token, uint8_t* send_buf, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    if (const moe_status cs = check_config(cfg); cs != MOE_OK) return cs;
+    if (R < 1 || R > cfg->E || cfg->E % R) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!topk_idx || !topk_gate || !xq || !xs || !send_offsets || !send_row_of || !send_token || !send_buf)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(xq) || !aligned16(send_buf) || !aligned16(topk_idx)) return MOE_ERR_INVALID_ARG;
+    const size_t need = moe_ep_workspace_size(cfg, R, cfg->T);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    const int nblk = static_cast<int>(ceil_div(cfg->T, perm::kTokPerBlk));
+    int32_t* blk_counts = static_cast<int32_t*>(workspace);
+    int32_t* blk_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + need / 2);
+    const cudaStream_t st = as_stream(stream);
+    const int64_t npairs = static_cast<int64_t>(cfg->T) * cfg->K;
+    const perm::KeyDest key{topk_idx, cfg->E, cfg->E / R};
+    const size_t hsm = static_cast<size_t>(perm::kWarps) * R * sizeof(int);
+    perm::hist_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(key, npairs, cfg->K, R, blk_counts);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    perm::scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, R, cfg->T, cfg->K, blk_base, send_offsets, send_counts,
+                                          false);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    perm::scatter_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(key, npairs, cfg->K, R, blk_base, send_row_of,
+                                                               send_token, false);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    // at most min(K, R) send rows per token; warps past the total stop at once
+    const int64_t cap = static_cast<int64_t>(cfg->T) * std::min(cfg->K, R);
+    ep::pack_kernel<<<static_cast<unsigned>(ceil_div(cap * 32, 256)), 256, 0, st>>>(
+        send_offsets + R, send_token, cap, cfg->T, cfg->d, cfg->K, xq, xs, topk_idx, topk_gate, send_buf);
+    return launch_status();
+}
+
+moe_status moe_ep_receive(const moe_config* cfg, int32_t R, int32_t rank, int64_t n_recv, const uint8_t* recv_buf,
+                          int32_t* local_offsets, int32_t* local_counts, int32_t* sorted_row, int32_t* row_of,
+                          uint8_t* xq_local, float* xs_local, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    if (const moe_status cs = check_config(cfg); cs != MOE_OK) return cs;
+    if (R < 1 || R > cfg->E || cfg->E % R || rank < 0 || rank >= R || n_recv < 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (n_recv * cfg->K >= INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!local_offsets || !sorted_row || !row_of || !xq_local || !xs_local || (n_recv > 0 && !recv_buf))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(xq_local) || (recv_buf && !aligned16(recv_buf))) return MOE_ERR_INVALID_ARG;
+    const size_t need = moe_ep_workspace_size(cfg, R, n_recv);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    const int n_local = cfg->E / R;
+    const int nblk = static_cast<int>(ceil_div(std::max<int64_t>(n_recv, 1), perm::kTokPerBlk));
+    int32_t* blk_counts = static_cast<int32_t*>(workspace);
+    int32_t* blk_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + need / 2);
+    const cudaStream_t st = as_stream(stream);
+    const int64_t npairs = n_recv * cfg->K;
+    const int64_t rb = ep::row_bytes(cfg->d, cfg->K);
+    const int32_t* ridx =
+        recv_buf != nullptr ? reinterpret_cast<const int32_t*>(recv_buf + cfg->d + 4 * (cfg->d / 128)) : nullptr;
+    const perm::KeyWindow key{ridx, rb / 4, cfg->E, rank * n_local, n_local};
+    const size_t hsm = static_cast<size_t>(perm::kWarps) * n_local * sizeof(int);
+    perm::hist_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(key, npairs, cfg->K, n_local, blk_counts);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    perm::scan_kernel<<<1, 1024, 0, st>>>(blk_counts, nblk, n_local, static_cast<int>(n_recv), cfg->K, blk_base,
+                                          local_offsets, local_counts, false);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (n_recv == 0) return MOE_OK;
+    perm::scatter_kernel<<<nblk, perm::kWarps * 32, hsm, st>>>(key, npairs, cfg->K, n_local, blk_base, row_of,
+                                                               sorted_row, false);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    ep::gather_kernel<<<static_cast<unsigned>(ceil_div(npairs * 32, 256)), 256, 0, st>>>(
+        local_offsets, n_local, sorted_row, n_recv, recv_buf, cfg->d, cfg->K, xq_local, xs_local);
+    return launch_status();
+}
+
+moe_status moe_ep_partial(const moe_config* cfg, int64_t n_recv, const uint8_t* recv_buf, const int32_t* row_of,
+                          const uint16_t* routed_out, int64_t out_rows, float* partial, void* stream) {
+    if (const moe_status cs = check_config(cfg); cs != MOE_OK) return cs;
+    if (n_recv < 0 || out_rows < 0 || n_recv > INT32_MAX) return MOE_ERR_INVALID_ARG;
+    if (n_recv == 0) return MOE_OK;
+    if (!recv_buf || !row_of || !routed_out || !partial) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(recv_buf) || !aligned16(routed_out) || !aligned16(partial)) return MOE_ERR_INVALID_ARG;
+    ep::partial_kernel<<<static_cast<unsigned>(n_recv), 256, 0, as_stream(stream)>>>(recv_buf, cfg->d, cfg->K, row_of,
+                                                                                     out_rows, routed_out, partial);
+    return launch_status();
+}
+
+moe_status moe_ep_combine(const moe_config* cfg, const float* shared_out, const float* returned, int64_t S,
+                          const int32_t* send_row_of, const uint16_t* residual, uint16_t* y, void* stream) {
+    if (const moe_status cs = check_config(cfg); cs != MOE_OK) return cs;
+    if (!shared_out || !send_row_of || !y || S < 0 || (S > 0 && !returned)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(shared_out) || !aligned16(y) || (returned && !aligned16(returned)) ||
+        (residual && !aligned16(residual)))
+        return MOE_ERR_INVALID_ARG;
+    ep::combine_kernel<<<cfg->T, 256, 0, as_stream(stream)>>>(shared_out, returned, send_row_of, S, residual, cfg->T,
+                                                              cfg->K, cfg->d, y);
     return launch_status();
 }
 

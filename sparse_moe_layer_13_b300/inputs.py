@@ -9,7 +9,8 @@ Recipe (all draws from ``torch.Generator`` seeded per tensor):
 * x       : bf16 [T][d], N(0, 1) drawn in fp32 then rounded to bf16 (RNE).
 * Wr      : fp32 [E][d], N(0, 1/d).
 * bias    : fp32 [E], zeros or U(-0.1, 0.1).
-* W1, W3  : fp32 [I][d] per expert, N(0, 1/d) (gate and up projections).
+* W1, W3  : fp32 [I][d] per expert, N(0, 1/d) (gate and up projections),
+  seeded by the workload's expert seed (the full-width workloads share one).
 * W2      : fp32 [d][I] per expert, N(0, 1/d) (down projection).
 * dy      : bf16 [T][d], N(0, 1), the upstream gradient of a backward pass.
 * logit offsets (skewed workload only): o_e = -c * s * ln(rank_e) with rank a
@@ -61,11 +62,13 @@ def gen_bias(cfg: MoEConfig, device="cpu") -> torch.Tensor:
 
 
 def gen_expert(cfg: MoEConfig, e: int, device="cpu"):
-    """fp32 (W1 [I][d], W3 [I][d], W2 [d][I]) of expert e; e == E is the shared expert."""
+    """fp32 (W1 [I][d], W3 [I][d], W2 [d][I]) of expert e; e == E is the shared expert.
+    Drawn from the workload's expert seed (cfg.weight_seed)."""
     s = 1.0 / math.sqrt(cfg.d)
-    w1 = torch.randn(cfg.I, cfg.d, generator=_gen(cfg.seed, "w1", e, device), device=device) * s
-    w3 = torch.randn(cfg.I, cfg.d, generator=_gen(cfg.seed, "w3", e, device), device=device) * s
-    w2 = torch.randn(cfg.d, cfg.I, generator=_gen(cfg.seed, "w2", e, device), device=device) * s
+    ws = cfg.weight_seed
+    w1 = torch.randn(cfg.I, cfg.d, generator=_gen(ws, "w1", e, device), device=device) * s
+    w3 = torch.randn(cfg.I, cfg.d, generator=_gen(ws, "w3", e, device), device=device) * s
+    w2 = torch.randn(cfg.d, cfg.I, generator=_gen(ws, "w2", e, device), device=device) * s
     return w1, w3, w2
 
 

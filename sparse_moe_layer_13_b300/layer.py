@@ -2,7 +2,7 @@
 
 《DeepSeek-V3 Technical Report》深度解读报告 §2.2-§2.4 and "DeepSeek-V3的MoE架构
 设计革新" §2 describe the layer; this module only owns device buffers and
-calls, in order: moe_route -> moe_permute (row order only) ->
+calls, in order: moe_route_planes -> moe_permute (row order only) ->
 moe_quant_fp8_1x128_scatter (tokens quantised straight into grouped rows) ->
 moe_grouped_gemm_fp8 (gate/up + SwiGLU + requantisation) ->
 moe_grouped_gemm_fp8 (down) -> moe_combine -> moe_bias_update. Expert E (the
@@ -91,6 +91,7 @@ class MoELayer:
         self.block_scaled = scale_rule == "pow2"
         self.device = device
         self.Wr = inputs.gen_router(cfg, device)
+        self.planes = B.router_planes(self.Wr)        # redo with refresh_router() when Wr changes
         self.bias = inputs.gen_bias(cfg, device)
         self.logit_offset = logit_offset
         self.w = ExpertWeights(cfg, device, scale_rule=scale_rule, backward=backward) if weights is None else weights
@@ -132,20 +133,33 @@ class MoELayer:
         T*K/E the update judges each expert. It defaults to this layer's T
         without a hook and to dp.global_tokens(T) with one (every rank of the
         default group holding T tokens). events, if given, is a dict of
-        name -> (start, end) torch.cuda.Event pairs recorded around the two
-        grouped GEMMs ("gemm1", "gemm2"); out, if given, receives y (bf16
-        [T][d]) instead of the layer's own buffer.
+        name -> (start, end) torch.cuda.Event pairs recorded around the calls
+        "route" (router with loads), "permute" (row order), "quant" (quantise
+        into grouped rows, token_rows "scatter"), "gemm1" (gate/up + SwiGLU),
+        "gemm2" (down) and "combine"; out, if given, receives y (bf16 [T][d])
+        instead of the layer's own buffer.
         """
         c = self.cfg
         ev = events or {}
-        B.route(c, x, self.Wr, self.bias, self.logit_offset, self.ws, self.idx, self.gate, self.counts)
+
+        def mark(name, i):
+            if name in ev:
+                ev[name][i].record()
+
+        mark("route", 0)
+        B.route_planes(c, x, self.planes, self.bias, self.logit_offset, self.ws, self.idx, self.gate, self.counts)
+        mark("route", 1)
         mode = self.token_rows
         rule = self.scale_rule
         if mode != "scatter":
             B.quant_1x128(x, self.xq, self.xs, rule=rule)
+        mark("permute", 0)
         B.permute(c, self.idx, self.xq, self.xs, self.ws, self.perm, gather_rows=mode == "copy")
+        mark("permute", 1)
         if mode == "scatter":
+            mark("quant", 0)
             B.quant_1x128_scatter(c, x, self.perm["row_of"], self.xq_perm, self.xs_perm, rule=rule)
+            mark("quant", 1)
         if "gemm1" in ev:
             ev["gemm1"][0].record()
         if mode == "gather":
@@ -164,10 +178,16 @@ class MoELayer:
             ev["gemm2"][1].record()
         TK = c.T * c.K
         y = self.y if out is None else out
+        mark("combine", 0)
         B.combine(c, self.out[:TK], self.out_shared, self.perm["row_of"], self.gate, x if residual else None, y)
+        mark("combine", 1)
         if update_bias:
             self.end_of_step(gamma, counts_hook, load_tokens)
         return y
+
+    def refresh_router(self):
+        """Re-splits the router weight into the bf16 planes the router reads (after Wr changed)."""
+        B.router_planes(self.Wr, self.planes)
 
     def end_of_step(self, gamma: float | None = None, counts_hook=None, load_tokens: int | None = None):
         """The end-of-step bias update on the last routing's expert load
@@ -294,9 +314,16 @@ class MoELayer:
                 self.forward(x, events=None if events is None else events[i], **forward_kw)
         return graph
 
-    # library kernel launches per forward: route 5 (weight split, logits, selection, histogram,
-    # scan), quantise 1, permute 3 (+1 row gather for "copy"), grouped GEMMs 2, combine 1,
-    # bias update 1
+    # library kernel launches per forward: route 3 (fused router, histogram, scan) or 4 on the
+    # K-split path (logits, selection, histogram, scan), quantise 1, permute 3 (+1 row gather
+    # for "copy"), grouped GEMMs 2, combine 1, bias update 1
+    @property
+    def route_fused(self) -> bool:
+        """Whether moe_route_planes' automatic choice takes the fused router for this layer."""
+        c = self.cfg
+        sms = torch.cuda.get_device_properties(torch.device(self.device)).multi_processor_count
+        return c.E <= 256 and 2 * ((c.T + 127) // 128) >= sms
+
     @property
     def launches_per_forward(self) -> int:
-        return 13 + int(self.token_rows == "copy")
+        return (3 if self.route_fused else 4) + 8 + int(self.token_rows == "copy")

@@ -49,16 +49,42 @@ def assert_y_close(got, want):
     return rel, mx
 
 
-def oracle_experts(cfg, experts, device="cuda", rule="fp32"):
+# Oracle experts quantised so far in this test session, keyed by (expert seed,
+# d, I, scale rule, expert): the full-width workloads share one set of expert
+# weights, so their tests quantise each expert once.
+_EXPERTS: dict = {}
+
+
+def oracle_experts(cfg, experts, device="cuda", rule="fp32", batch: int = 48):
     """Quantised oracle experts for `experts`, built in parallel CPU workers.
 
     The fp32 weights come from the same seeded generator (on `device`) that
-    fed the CUDA path; the workers run only the oracle's quantiser.
+    fed the CUDA path; the workers run only the oracle's quantiser. Weights
+    are drawn `batch` experts at a time to bound host memory.
     """
     from oracle.parallel import quantize_experts
     from sparse_moe_layer_13_b300.inputs import gen_expert
-    jobs = [(e, *(to_np(w) for w in gen_expert(cfg, e, device))) for e in sorted(set(int(e) for e in experts))]
-    return quantize_experts(jobs, rule=rule)
+    key = (cfg.weight_seed, cfg.d, cfg.I, rule)
+    want = sorted(set(int(e) for e in experts))
+    missing = [e for e in want if key + (e,) not in _EXPERTS]
+    for i in range(0, len(missing), batch):
+        jobs = [(e, *(to_np(w) for w in gen_expert(cfg, e, device))) for e in missing[i:i + batch]]
+        for e, q in quantize_experts(jobs, rule=rule).items():
+            _EXPERTS[key + (e,)] = q
+        del jobs
+    return {e: _EXPERTS[key + (e,)] for e in want}
+
+
+def oracle_route_chunked(x, Wr, bias, cfg, logit_offset=None, chunk: int = 8192):
+    """The oracle router over a large batch, a slice of tokens at a time (routing is
+    per token, so this is the same function; it only bounds the FP64 copies)."""
+    from oracle.route import route as oracle_route
+    parts = [oracle_route(np.asarray(x[i:i + chunk], np.float32), Wr, bias, cfg.G, cfg.M, cfg.K, cfg.gk,
+                          logit_offset) for i in range(0, x.shape[0], chunk)]
+    idx = np.concatenate([p[0] for p in parts])
+    gate = np.concatenate([p[1] for p in parts])
+    info = {k: np.concatenate([p[2][k] for p in parts]) for k in parts[0][2]}
+    return idx, gate, info
 
 
 def check_routing(cfg, idx_gpu, gate_gpu, ref_idx, ref_gate, info):
@@ -78,3 +104,25 @@ def check_routing(cfg, idx_gpu, gate_gpu, ref_idx, ref_gate, info):
     err = np.abs(g1 - g2).max() if g1.size else 0.0
     assert err <= GATE_ATOL, f"gate error {err:.3e}"
     return tie, err
+
+
+def check_load_and_bias(cfg, gpu_idx, gpu_counts, ref_idx, tie, b0, bias_after, T=None):
+    """End-of-step checks (《DeepSeek-V3 Technical Report》深度解读报告 §2.3), every call:
+    the device histogram is exactly that of the device's choice; with the near-tie tokens
+    taken out of both, it equals the oracle's load; and the updated bias is, bit for bit,
+    the update rule applied to the device's load."""
+    from oracle.layer import bias_update
+    T = cfg.T if T is None else T
+
+    def histogram(idx, E):          # a library count (the oracle's own histogram is pinned to it)
+        return np.bincount(np.asarray(idx).ravel(), minlength=E).astype(np.int32)
+
+    assert np.array_equal(gpu_counts, histogram(gpu_idx, cfg.E))
+    assert np.array_equal(histogram(gpu_idx[~tie], cfg.E), histogram(ref_idx[~tie], cfg.E))
+    assert np.array_equal(bias_after, bias_update(b0, gpu_counts, T, cfg.K, cfg.gamma))
+    # the oracle's own load gives the same bias except where near-tie tokens can move an
+    # expert's load across the mean
+    ob = bias_update(b0, histogram(ref_idx, cfg.E), T, cfg.K, cfg.gamma)
+    moved = np.zeros(cfg.E, bool)
+    moved[np.unique(np.concatenate([gpu_idx[tie].ravel(), ref_idx[tie].ravel()]))] = True
+    assert np.all((ob == bias_after) | moved)

@@ -81,6 +81,15 @@ def test_host_side_errors_return_before_launch(lib):
     # workspace too small
     assert lib.moe_permute(ctypes.byref(c), fake, fake, fake, fake, None, fake, fake, fake, fake, fake, 16, None) == 3
     assert lib.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, fake, None, None, 0, None) == 3
+    # router on weight planes: bad path enum, fused path beyond 256 experts, small workspace, null weight
+    from sparse_moe_layer_13_b300.configs import MoEConfig
+    big = binding.config_c(MoEConfig("e512", T=64, d=128, E=512, I=128, K=8, G=8, M=4, gk=2, seed=1))
+    huge = 1 << 40
+    assert lib.moe_route_planes(ctypes.byref(c), fake, fake, None, fake, fake, fake, None, 7, fake, huge, None) == 1
+    assert lib.moe_route_planes(ctypes.byref(big), fake, fake, None, fake, fake, fake, None, 1, fake, huge, None) == 2
+    assert lib.moe_route_planes(ctypes.byref(c), fake, fake, None, fake, fake, fake, None, 0, fake, 16, None) == 3
+    assert lib.moe_route_planes(ctypes.byref(c), fake, None, None, fake, fake, fake, None, 0, fake, huge, None) == 1
+    assert lib.moe_router_planes(None, 16, 256, fake, None) == 1
 
 
 def test_backward_host_side_errors_return_before_launch(lib):
@@ -120,3 +129,30 @@ def test_backward_host_side_errors_return_before_launch(lib):
     assert lib.moe_grouped_wgrad_fp8(2, fake, 64, 512, 128, 256, fake, fake, fake, fake, not32, None) == 1
     # the gate/up FP32 epilogue has no block-scaled variant
     assert lib.moe_grouped_gemm_fp8_mx(4, fake, 100, 256, 256, fake, fake, fake, fake, 4, fake, None, None) == 2
+
+
+def test_expert_parallel_host_side_checks(lib):
+    """Expert-parallel entry points: packed row size, workspace query, and rejects of a
+    rank count that does not split the experts, bad ranks, null pointers and small
+    workspaces, all before any launch."""
+    from sparse_moe_layer_13_b300 import binding
+    from sparse_moe_layer_13_b300.configs import TINY
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    c = ctypes.byref(binding.config_c(TINY))            # E = 16, K = 4, d = 256
+    # 256 code bytes + 2 scales * 4 + 4 ids * 4 + 4 gates * 4 = 296 -> 304
+    assert lib.moe_ep_row_bytes(256, 4) == 304
+    assert lib.moe_ep_row_bytes(7168, 8) == 7168 + 224 + 64
+    assert lib.moe_ep_row_bytes(100, 4) == 0 and lib.moe_ep_row_bytes(256, 17) == 0
+    assert lib.moe_ep_workspace_size(c, 3, 256) == 0      # 16 experts do not split over 3 ranks
+    assert lib.moe_ep_workspace_size(c, 4, 256) > 0
+    big = 1 << 40
+    assert lib.moe_ep_dispatch(c, 3, fake, fake, fake, fake, None, fake, fake, fake, fake, fake, big, None) == 2
+    assert lib.moe_ep_dispatch(c, 4, None, fake, fake, fake, None, fake, fake, fake, fake, fake, big, None) == 1
+    assert lib.moe_ep_dispatch(c, 4, fake, fake, fake, fake, None, fake, fake, fake, fake, fake, 16, None) == 3
+    assert lib.moe_ep_receive(c, 4, 4, 10, fake, fake, None, fake, fake, fake, fake, fake, big, None) == 2
+    assert lib.moe_ep_receive(c, 4, 0, 10, None, fake, None, fake, fake, fake, fake, fake, big, None) == 1
+    assert lib.moe_ep_receive(c, 4, 0, 10, fake, fake, None, fake, fake, fake, fake, fake, 16, None) == 3
+    assert lib.moe_ep_partial(c, 5, None, fake, fake, 10, fake, None) == 1
+    assert lib.moe_ep_combine(c, None, fake, 10, fake, None, fake, None) == 1
+    assert lib.moe_ep_combine(c, fake, None, 10, fake, None, fake, None) == 1

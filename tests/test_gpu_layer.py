@@ -6,9 +6,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_y_close, check_routing, gpu, oracle_experts, require_gpu, to_np
-from oracle.layer import Layer, bias_update
-from oracle.permute import histogram
+from gpu_helpers import assert_y_close, check_load_and_bias, check_routing, gpu, oracle_experts, require_gpu, to_np
+from oracle.layer import Layer
 from oracle.route import near_tie, route as oracle_route
 from sparse_moe_layer_13_b300.configs import CONFIGS
 
@@ -36,10 +35,7 @@ def _layer_case(cfg, n_sample=None, residual=False, seed=0, rule="fp32"):
                                                                   residual=residual)
     keep = ~tie[tokens]
     rel, mx = assert_y_close(y[tokens][keep], ref["y"][keep])
-    # end-of-step bias update, bit-exact, from the oracle's own load
-    if not tie.any():
-        want_b = bias_update(b0, histogram(ref_idx, cfg.E), cfg.T, cfg.K, cfg.gamma)
-        assert np.array_equal(to_np(layer.bias), want_b)
+    check_load_and_bias(cfg, to_np(layer.idx), to_np(layer.counts), ref_idx, tie, b0, to_np(layer.bias))
     return rel, mx, layer
 
 
@@ -62,15 +58,15 @@ def test_layer_mid():
 
 
 @gpu
-def test_layer_decode_sampled():
+def test_layer_decode_every_token():
     require_gpu()
-    _layer_case(CONFIGS["decode"], n_sample=6, seed=1)
+    _layer_case(CONFIGS["decode"])
 
 
 @gpu
 def test_layer_full_width_prefill_sampled():
     require_gpu()
-    _layer_case(CONFIGS["full"], n_sample=6, seed=2)
+    _layer_case(CONFIGS["full"], n_sample=64, seed=2)
 
 
 @gpu

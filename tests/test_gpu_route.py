@@ -84,3 +84,88 @@ def test_balance_loss_matches_oracle(name, seq_len):
     assert np.allclose(to_np(f), rf, rtol=1e-6, atol=0)          # counts exact; E / (K L) rounded in FP32
     assert np.allclose(to_np(P), rP, rtol=1e-5, atol=1e-9)
     assert np.allclose(to_np(loss), 1e-4 * (rf * rP).sum(axis=1), rtol=1e-5, atol=0)
+
+
+def _stored_logits(cfg, ws):
+    """The logits the router left in the workspace: (split count word, summed logits [T][E]),
+    the K-split partials summed in split order in FP32 as the kernels add them."""
+    raw = ws.cpu().numpy()
+    splits = int(raw[:4].view(np.int32)[0])
+    z = raw[256:256 + splits * cfg.T * cfg.E * 4].view(np.float32).reshape(splits, cfg.T, cfg.E)
+    acc = z[0].copy()
+    for s in range(1, splits):
+        acc = (acc + z[s]).astype(np.float32)
+    return splits, acc
+
+
+@gpu
+@pytest.mark.parametrize("T", [16384, 16384 + 37])
+def test_route_fused_equals_split_path_bit_for_bit(T):
+    """At full width both router paths use 14 K splits, so the fused kernel's in-register
+    sums must equal the split path's stored partials summed in order: identical logits,
+    choice, gates and loads."""
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding, inputs
+    cfg = CONFIGS["full"].with_tokens(T)
+    x = inputs.gen_x(cfg, "cuda")
+    Wr = inputs.gen_router(cfg, "cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    bias = (torch.rand(cfg.E, generator=g, device="cuda") - 0.5) * 0.02
+    planes = binding.router_planes(Wr)
+    out = {}
+    for path in ("split", "fused"):
+        ws = torch.zeros(binding.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+        idx, gate, counts = binding.route_planes(cfg, x, planes, bias, workspace=ws, want_counts=True, path=path)
+        binding.check_device_status()
+        out[path] = (idx, gate, counts, *_stored_logits(cfg, ws))
+    assert out["split"][3] == 14 and out["fused"][3] == 1
+    assert np.array_equal(out["split"][4], out["fused"][4])
+    for i in range(3):
+        assert torch.equal(out["split"][i], out["fused"][i])
+
+
+@gpu
+@pytest.mark.parametrize("name,T", [("tiny", None), ("tiny", 300), ("mid", None), ("mid", 1)])
+def test_route_fused_path_matches_oracle(name, T):
+    """The fused router forced on shapes where the automatic choice takes the split path
+    (few token tiles, E = 16 and 64, a ragged tail, a single token)."""
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding, inputs
+    c = CONFIGS[name] if T is None else CONFIGS[name].with_tokens(T)
+    x = inputs.gen_x(c, "cuda")
+    Wr = inputs.gen_router(c, "cuda")
+    b = inputs.gen_bias(c, "cuda")
+    idx, gate, counts = binding.route_planes(c, x, binding.router_planes(Wr), b, want_counts=True, path="fused")
+    binding.check_device_status()
+    ref_idx, ref_gate, info = oracle_route(to_np(x), to_np(Wr), to_np(b), c.G, c.M, c.K, c.gk)
+    check_routing(c, to_np(idx), to_np(gate), ref_idx, ref_gate, info)
+    assert np.array_equal(to_np(counts), histogram(to_np(idx), c.E))
+
+
+@gpu
+def test_route_fused_all_experts_one_group():
+    """Fused path on the degenerate selections: K = E (every expert chosen) and G = 1."""
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding, inputs
+    for c in (MoEConfig("allk", T=200, d=256, E=16, I=128, K=16, G=2, M=2, gk=1, seed=9, bias="uniform"),
+              MoEConfig("g1", T=130, d=128, E=32, I=128, K=5, G=1, M=1, gk=3, seed=10, bias="uniform")):
+        x = inputs.gen_x(c, "cuda")
+        Wr = inputs.gen_router(c, "cuda")
+        b = inputs.gen_bias(c, "cuda")
+        idx, gate, _ = binding.route_planes(c, x, binding.router_planes(Wr), b, path="fused")
+        binding.check_device_status()
+        ref_idx, ref_gate, info = oracle_route(to_np(x), to_np(Wr), to_np(b), c.G, c.M, c.K, c.gk)
+        check_routing(c, to_np(idx), to_np(gate), ref_idx, ref_gate, info)
+
+
+@gpu
+def test_route_planes_rejects_fused_beyond_256_experts():
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding, inputs
+    c = MoEConfig("e512", T=64, d=128, E=512, I=128, K=8, G=8, M=4, gk=2, seed=12)
+    x = inputs.gen_x(c, "cuda")
+    Wr = inputs.gen_router(c, "cuda")
+    with pytest.raises(binding.MoeError) as e:
+        binding.route_planes(c, x, binding.router_planes(Wr), torch.zeros(c.E, device="cuda"), path="fused")
+    assert e.value.code == 2
