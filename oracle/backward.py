@@ -43,6 +43,7 @@ import numpy as np
 
 from . import e4m3
 from .ffn import silu
+from .bounds import ARITH_ULPS, U, gate_err, gemm_bound, silu_derivs, swiglu_h_bound, tile_range
 from .quant import TILE, dequant_1x128, quant_1x128
 
 
@@ -106,108 +107,81 @@ def _fl32(v) -> np.ndarray:
     return np.asarray(v, np.float64).astype(np.float32)
 
 
-NEAR_TOL = 3e-5
-
-
-def near_midpoint(ratio, tol: float = NEAR_TOL) -> np.ndarray:
-    """Elements whose quantisation ratio v / scale lies within tol (relative) of
-    a rounding midpoint of the E4M3 grid: a perturbation of v that small may
-    round it to the neighbouring code. The default tol covers two evaluations
-    of the same gradient element whose GEMM sums were accumulated
-    differently (an FP8 tensor-core chunk product may be summed with less
-    than FP32's 24-bit precision before its promotion, the reason the pages
-    give for promoting every 128 elements)."""
-    r = np.abs(np.asarray(ratio, np.float64))
-    r = np.minimum(r, e4m3.E4M3_MAX)
-    with np.errstate(divide="ignore"):
-        e = np.maximum(np.floor(np.log2(np.where(r > 0, r, 1.0))), -6)
-    sp = np.ldexp(1.0, (e - 3).astype(np.int64))
-    mid = (np.floor(r / sp) + 0.5) * sp
-    return (r > 0) & (np.abs(r - mid) < tol * r)
+# ------------------------------------------------------ evaluation bounds ----
+# Two correct FP32 evaluations of the same gradient may straddle an E4M3
+# rounding boundary (oracle/bounds.py). For each quantised operand the
+# functions below carry a bound on how far a correct evaluation's input may
+# lie from the oracle's ("err"), turn it into the range of dequantised values
+# such an evaluation may produce ("delta"), and propagate the ranges linearly
+# into "budgets" on the gradients.
 
 
 class Quantiser:
     """The quantisation points of the backward; identity when `on` is False.
 
-    Each call records in `near` the elements that sit within `tol` of an E4M3
-    rounding midpoint while one E4M3 step of them is more than `sig` of the
-    norm of their tile's row or column (the line the quantised values feed):
-    where another correct FP32 evaluation of the same value may pick a
-    neighbouring code that matters. near_rows / near_cols: any per row /
-    column."""
+    Each call takes the values v (the oracle's, rounded to FP32 where the device stores FP32)
+    and err, a bound on how far another correct evaluation's v may lie from them, and records
+    in `delta` the width of the range of dequantised values such an evaluation may produce
+    (zero where err is zero: the same bits on both sides)."""
 
-    def __init__(self, rule: str = "fp32", on: bool = True, tol: float = NEAR_TOL, sig: float = 2e-3):
+    def __init__(self, rule: str = "fp32", on: bool = True):
         self.rule = rule
         self.on = on
-        self.tol = tol
-        self.sig = sig
-        self.near = None
+        self.delta = None
+        self.row_rel = None     # scaled_rows under the FP32 rule: the range is a uniform scaling per row
 
-    @property
-    def near_rows(self):
-        return self.near.any(axis=1)
-
-    @property
-    def near_cols(self):
-        return self.near.any(axis=0)
-
-    def _flag(self, v32, sc, deq, axis):
-        with np.errstate(divide="ignore", invalid="ignore"):
-            ratio = np.where(sc > 0, v32.astype(np.float64) / sc, 0.0)
-        r = np.minimum(np.abs(ratio), e4m3.E4M3_MAX)
-        with np.errstate(divide="ignore"):
-            e = np.maximum(np.floor(np.log2(np.where(r > 0, r, 1.0))), -6)
-        step = np.ldexp(1.0, (e - 3).astype(np.int64)) * sc          # one E4M3 step, in value units
-        self.near_raw = near_midpoint(ratio, self.tol)
-        self.step = step
-        return self.near_raw & self.significant(step, deq, axis)
-
-    def significant(self, step, deq, axis):
-        """Steps larger than `sig` of the norm of their line (row: axis 1, column: axis 0) of deq."""
-        norm = np.linalg.norm(deq, axis=axis, keepdims=True)
-        return step > self.sig * np.where(norm > 0, norm, np.inf)
-
-    def rows(self, v) -> np.ndarray:
+    def rows(self, v, err=0.0) -> np.ndarray:
         """1x128 tiles along the last axis (after rounding to FP32), dequantised."""
         if not self.on:
-            self.near = np.zeros(np.shape(v), bool)
-            self.near_raw, self.step = self.near, np.zeros(np.shape(v))
+            self.delta = np.zeros(np.shape(v))
             return np.asarray(v, np.float64)
         v32 = _fl32(v)
         q, s = quant_1x128(v32, self.rule)
         deq = dequant_1x128(q, s)
-        self.near = self._flag(v32, np.repeat(s, TILE, axis=1), deq, axis=1)
+        lo, hi = tile_range(v32, err, self.rule)
+        self.delta = np.maximum(hi, deq) - np.minimum(lo, deq)
         return deq
 
-    def scaled_rows(self, y, g) -> np.ndarray:
-        """The 1x128 quantisation of g[i] * y[i] (g > 0 per row), dequantised.
+    def scaled_rows(self, y, g, g_err=0.0) -> np.ndarray:
+        """The 1x128 quantisation of g[i] * y[i] (g > 0 per row), dequantised; g may be off by g_err.
 
-        FP32 rule: g scales each tile uniformly, so the codes are those of y's
-        own tiles and the scale is fl32(g * s_y). (Quantising fl32(g * y) again
-        would leave the ratios 448 * y / max|y| -- often exact E4M3 midpoints
-        for bf16 y -- to be decided by g's last bit.) Power-of-two rule: a
-        power-of-two scale cannot absorb g, so fl32(g * y) is quantised.
-        Nothing is flagged in the FP32 case: the codes come from y alone.
+        FP32 rule: g scales each tile uniformly, so the codes are those of y's own tiles and
+        the scale is fl32(g * s_y); a gate off by g_err moves every dequantised value by the
+        same relative amount (no code changes). (Quantising fl32(g * y) again would leave
+        the ratios 448 * y / max|y| -- often exact E4M3 midpoints for bf16 y -- to be
+        decided by g's last bit.) Power-of-two rule: a power-of-two scale cannot absorb g,
+        so fl32(g * y) is quantised, each value off by |y| * g_err.
         """
         y = np.asarray(y, np.float64)
         g = np.asarray(g, np.float64).reshape(-1, 1)
-        if not self.on or self.rule != "fp32":
-            return self.rows(g * y if not self.on else _fl32(g * y))
+        ge = np.broadcast_to(np.asarray(g_err, np.float64).reshape(-1, 1) if np.ndim(g_err) else g_err, g.shape)
+        if not self.on:
+            self.delta = np.zeros(y.shape)
+            return g * y
+        if self.rule != "fp32":
+            return self.rows(_fl32(g * y), np.abs(y) * ge + U * np.abs(g * y))
         q, s = quant_1x128(_fl32(y), self.rule)
-        self.near = np.zeros(y.shape, bool)
-        return dequant_1x128(q, (g * s.astype(np.float64)).astype(np.float32))
+        deq = dequant_1x128(q, (g * s.astype(np.float64)).astype(np.float32))
+        self.row_rel = (2.0 * (ge / g + U)).ravel()       # every value of a row moves by this relative range
+        self.delta = np.abs(deq) * self.row_rel[:, None]
+        return deq
 
-    def tokens(self, v) -> np.ndarray:
+    def tokens(self, v, err=0.0) -> np.ndarray:
         """128x1 tiles along the first axis (one group of rows), dequantised: [m][C] float64."""
         if not self.on:
-            self.near = np.zeros(np.shape(v), bool)
+            self.delta = np.zeros(np.shape(v))
             return np.asarray(v, np.float64)
         v = _fl32(v)
-        m = v.shape[0]
+        m, C = v.shape
         qT, sT = quant_128x1_grouped(v, [0, m], self.rule)
         deq = dequant_128x1_grouped(qT, sT)[:, :m].T
-        sc = np.repeat(sT, TILE, axis=0)[:m]
-        self.near = self._flag(v, sc, deq, axis=0)
+        mp = qT.shape[1]
+        pad = np.zeros((mp, C))
+        pad[:m] = v
+        epad = np.zeros((mp, C))
+        epad[:m] = np.broadcast_to(np.asarray(err, np.float64), v.shape)
+        lo, hi = tile_range(pad.T, epad.T, self.rule)
+        self.delta = (np.maximum(hi.T[:m], deq) - np.minimum(lo.T[:m], deq))
         return deq
 
 
@@ -231,63 +205,83 @@ def gate_grad(s_sel, dg):
     return ds * s_sel * (1.0 - s_sel)
 
 
-def expert_dgrad(xd, W1, W3, W2, dO, Q: Quantiser, dO_exact: bool = False, dOd=None) -> dict:
+def expert_dgrad(xd, W1, W3, W2, dOd, Q: Quantiser, dOd_delta=None, dOd_row_rel=None) -> dict:
     """Rows of one expert: forward recomputation and data gradient.
 
-    xd [m][d] the expert's input rows as the forward multiplied them
-    (dequantised FP8); W1, W3 [I][d], W2 [d][I] the weights as the forward used
-    them (dequantised blocks); dO [m][d] the gradient of the expert output
-    (dO_exact: its values are inputs, not computed, so never flagged); dOd,
-    if given, is dO already quantised for the data gradient (Quantiser.scaled_rows).
+    xd [m][d] the expert's input rows as the forward multiplied them (dequantised FP8; the
+    same bits on every side); W1, W3 [I][d], W2 [d][I] the weights as the forward used them
+    (dequantised blocks); dOd [m][d] the expert-output gradient as the data-gradient GEMM
+    quantised it (Quantiser.scaled_rows), with either dOd_row_rel, the relative range of a
+    whole row scaled uniformly (the FP32 rule: a gate error rescales the row, so dh moves by
+    the same relative amount), or dOd_delta, the range of each dequantised value.
+
+    With Q on, also the error bounds: e_a, e_b of the gate/up GEMM outputs, e_h of h (fast
+    SiLU), e_dh of the dh GEMM (plus the gate's effect through dOd_delta), e_dA, e_dB by
+    first-order sensitivities of the SwiGLU gradient, and the ranges delta_h, delta_dA,
+    delta_dB of the quantised h, dA, dB; budget_dx = delta_dA @ |W1| + delta_dB @ |W3|.
     """
     a = xd @ W1.T
     b = xd @ W3.T
-    hd = Q.rows(_fl32(silu(a) * b) if Q.on else silu(a) * b)
-    # h elements near a rounding midpoint, with their E4M3 step (judged in expert_wgrad against
-    # the token direction, along which they enter the W2 gradient)
-    near_h = (Q.near_raw.copy(), Q.step.copy()) if Q.on else None
-    near = Q.near_rows.copy()
-    out = hd @ W2.T
-    if dOd is None:
-        dh = Q.rows(dO) @ W2
-        if not dO_exact:             # dO = dy itself (shared expert): the same bits on every side
-            near |= Q.near_rows
+    sig, silu, d1, d2 = silu_derivs(a)
+    h = silu * b
+    d, I = xd.shape[1], W1.shape[0]
+    if Q.on:
+        e_a = gemm_bound(xd, W1.T, d // TILE)
+        e_b = gemm_bound(xd, W3.T, d // TILE)
+        e_h = swiglu_h_bound(a, b, e_a, e_b)
     else:
-        dh = dOd @ W2
+        e_a = e_b = e_h = np.zeros_like(a)
+    hd = Q.rows(_fl32(h) if Q.on else h, e_h)
+    delta_h = Q.delta
+    out = hd @ W2.T
+    dh = dOd @ W2
+    Ip = (I + 255) // 256 * 256                     # the dh GEMM runs over I padded to 256
+    if Q.on:
+        e_dh = gemm_bound(dOd, W2, Ip // TILE)
+        if dOd_row_rel is not None:
+            e_dh = e_dh + dOd_row_rel[:, None] * np.abs(dh)
+        elif dOd_delta is not None:
+            e_dh = e_dh + dOd_delta @ np.abs(W2)
+    else:
+        e_dh = np.zeros_like(dh)
     dA, dB = swiglu_grad(a, b, dh)
-    dAd = Q.rows(dA)
-    near |= Q.near_rows
-    dBd = Q.rows(dB)
-    near |= Q.near_rows
+    e_dA = np.abs(b * d1) * e_dh + np.abs(dh * d1) * e_b + np.abs(dh * b * d2) * e_a + ARITH_ULPS * U * np.abs(dA)
+    e_dB = np.abs(silu) * e_dh + np.abs(dh * d1) * e_a + ARITH_ULPS * U * np.abs(dB)
+    dAd = Q.rows(dA, e_dA)
+    delta_dA = Q.delta
+    dBd = Q.rows(dB, e_dB)
+    delta_dB = Q.delta
     dx = dAd @ W1 + dBd @ W3
-    # near: rows with a quantised element (h, dO, dA, dB) near a rounding midpoint (see Quantiser);
-    # near_h: (near-midpoint mask, E4M3 step) of the elements of h
-    return {"a": a, "b": b, "hd": hd, "out": out, "dh": dh, "dA": dA, "dB": dB, "dx": dx, "near": near,
-            "near_h": near_h}
+    budget_dx = delta_dA @ np.abs(W1) + delta_dB @ np.abs(W3)
+    return {"a": a, "b": b, "hd": hd, "out": out, "dh": dh, "dA": dA, "dB": dB, "dx": dx,
+            "e_dA": e_dA, "e_dB": e_dB, "delta_h": delta_h, "budget_dx": budget_dx}
 
 
-def expert_wgrad(xd, hd, dO, dA, dB, Q: Quantiser, near_h=None, dO_exact: bool = False):
-    """Weight gradients of one expert over all its rows (token order):
-    dW1 [I][d], dW3 [I][d], dW2 [d][I], and the flags of the gradient rows and
-    columns fed by an operand channel with an element near a rounding
-    midpoint (dA, dB, dO; h from near_h, the forward's own flags): a dict
-    dW1 / dW3 -> rows [I], dW2 -> (rows [d], columns [I])."""
-    xt = Q.tokens(xd)              # x's codes and scales are the same bits on both sides: no flags
-    dAt = Q.tokens(dA)
-    fA = Q.near_cols
-    dBt = Q.tokens(dB)
-    fB = Q.near_cols
-    dOt = Q.tokens(dO)
-    fO = Q.near_cols if not dO_exact else np.zeros(dO.shape[1], bool)
-    ht = Q.tokens(hd)
-    # h differs between evaluations: in its codes (near_h) and, through the tile scales of the
-    # forward's 1x128 quantisation, in every dequantised value (the 128x1 requantisation's flags)
-    fh = Q.near_cols.copy()
-    if near_h is not None:
-        raw, step = near_h
-        fh |= (raw & Q.significant(step, hd, axis=0)).any(axis=0)
-    flags = {"dW1": fA, "dW3": fB, "dW2": (fO, fh)}
-    return dAt.T @ xt, dBt.T @ xt, dOt.T @ ht, flags
+def expert_wgrad(xd, hd, dO, dA, dB, Q: Quantiser, delta_h=None, e_dO=0.0, e_dA=0.0, e_dB=0.0):
+    """Weight gradients of one expert over all its rows (token order): dW1 [I][d], dW3
+    [I][d], dW2 [d][I], and their budgets from the 128x1 operands' ranges: x's codes and
+    scales are the same bits on every side; dA, dB, dO enter with their error bounds; h
+    enters as the forward's dequantised E4M3 values, whose own range is delta_h. With Q on,
+    budgets["base"] bounds each gradient's own FP32 evaluation (gemm_bound over the
+    expert's 128-token chunks): a correct device result lies within budget + base of these
+    values, element by element."""
+    xt = Q.tokens(xd)
+    dAt = Q.tokens(dA, e_dA)
+    rA = Q.delta
+    dBt = Q.tokens(dB, e_dB)
+    rB = Q.delta
+    dOt = Q.tokens(dO, e_dO)
+    rO = Q.delta
+    ht = Q.tokens(hd, 0.0 if delta_h is None else delta_h)
+    rh = Q.delta
+    budgets = {"dW1": rA.T @ np.abs(xt), "dW3": rB.T @ np.abs(xt),
+               "dW2": rO.T @ np.abs(ht) + np.abs(dOt).T @ rh}
+    if Q.on:
+        # the contraction's own FP32 evaluation over the expert's 128-token chunks
+        nkc = (xd.shape[0] + TILE - 1) // TILE
+        budgets["base"] = {"dW1": gemm_bound(dAt.T, xt, nkc), "dW3": gemm_bound(dBt.T, xt, nkc),
+                           "dW2": gemm_bound(dOt.T, ht, nkc)}
+    return dAt.T @ xt, dBt.T @ xt, dOt.T @ ht, budgets
 
 
 # -------------------------------------------------------------- the layer ----
@@ -301,16 +295,19 @@ def layer_backward(cfg, x, dy, Wr, idx, s_sel, experts_w, tokens=(), wgrad_exper
                    Q: Quantiser | None = None, xd=None) -> dict:
     """Gradients of the layer for upstream dy, routing (idx, s_sel) held fixed.
 
-    The result's "near" flags the tokens (of `tokens`) one of whose expert
-    rows has a quantised element within Q.tol of an E4M3 rounding midpoint:
-    there another correct FP32 evaluation may pick the neighbouring code.
-
     x, dy [T][d]; Wr [E][d]; idx [T][K]; s_sel [T][K] the chosen experts' raw
     affinities. experts_w(e) -> (W1, W3, W2) float64 as the GEMMs use them
     (e == E: the shared expert). Evaluates dx and dz for `tokens`, the expert
     weight gradients for `wgrad_experts`, and the router weight rows dWr[e]
     for `router_experts`. xd (optional) is x as the expert GEMMs see it; by
     default the 1x128-quantised x (or x itself when Q is off).
+
+    "budget" (with Q on) holds, per gradient element, how far another correct
+    evaluation may lie from these values through its quantisation decisions
+    alone (see Quantiser and expert_dgrad): dx [tokens][d], dz and dg
+    [tokens][K], dWr {e: [d]}; the expert weight gradients' budgets are the
+    fourth entry of each dW[e]. Routing follows the gates' error bound
+    (gate_err): h enters dg = dy . out, dg enters dz, dz enters dx and dWr.
     """
     Q = Quantiser() if Q is None else Q
     T, K = idx.shape
@@ -318,7 +315,9 @@ def layer_backward(cfg, x, dy, Wr, idx, s_sel, experts_w, tokens=(), wgrad_exper
     x = np.asarray(x, np.float64)
     dy = np.asarray(dy, np.float64)
     idx = np.asarray(idx)
-    gate = np.asarray(s_sel, np.float64) / np.asarray(s_sel, np.float64).sum(axis=1, keepdims=True)
+    s64 = np.asarray(s_sel, np.float64)
+    gate = s64 / s64.sum(axis=1, keepdims=True)
+    ge = gate_err(s64) if Q.on else np.zeros_like(gate)
     if xd is None:
         xd = Q.rows(x)
     tokens = np.asarray(sorted(set(int(t) for t in tokens)), np.int64)
@@ -347,56 +346,84 @@ def layer_backward(cfg, x, dy, Wr, idx, s_sel, experts_w, tokens=(), wgrad_exper
 
     dx_rows: dict = {}
     out_rows: dict = {}
-    near_tok: set = set()
+    bdx_rows: dict = {}
+    bdg_rows: dict = {}
     grads_w: dict = {}
     for e, prs in sorted(pairs.items()):
         prs = sorted(prs)                                   # token order = the expert's row order
         tt = np.array([p[0] for p in prs])
         kk = np.array([p[1] for p in prs])
         dO = np.stack([dO_of(t, k) for t, k in prs])
-        dOd = Q.scaled_rows(dy[tt], gate[tt, kk])
+        dOd = Q.scaled_rows(dy[tt], gate[tt, kk], ge[tt, kk])
+        uniform = Q.on and Q.rule == "fp32"
         W1, W3, W2 = experts_w(e)
-        r = expert_dgrad(xd[tt], W1, W3, W2, dO, Q, dOd=dOd)
+        r = expert_dgrad(xd[tt], W1, W3, W2, dOd, Q, dOd_delta=None if uniform else Q.delta,
+                         dOd_row_rel=Q.row_rel if uniform else None)
+        bdg = (r["delta_h"] * np.abs(dy[tt] @ W2)).sum(axis=1)     # h's range through dg = dy . (h W2^T)
         for i, p in enumerate(prs):
             dx_rows[p] = r["dx"][i]
             out_rows[p] = r["out"][i]
-            if r["near"][i]:
-                near_tok.add(p[0])
+            bdx_rows[p] = r["budget_dx"][i]
+            bdg_rows[p] = bdg[i]
         if e in wgrad_experts:
-            grads_w[e] = expert_wgrad(xd[tt], r["hd"], dO, r["dA"], r["dB"], Q, r["near_h"])
+            e_dO = np.abs(dy[tt]) * ge[tt, kk][:, None] + U * np.abs(dO)
+            grads_w[e] = expert_wgrad(xd[tt], r["hd"], dO, r["dA"], r["dB"], Q, r["delta_h"], e_dO, r["e_dA"],
+                                      r["e_dB"])
     if shared_tok:
         st = np.array(sorted(shared_tok))
         W1, W3, W2 = experts_w(E)
-        r = expert_dgrad(xd[st], W1, W3, W2, dy[st] if not Q.on else _fl32(dy[st]), Q, dO_exact=True)
+        dys = _fl32(dy[st]) if Q.on else dy[st]
+        dOd = Q.rows(dys)                                   # dy itself: the same bits on every side
+        r = expert_dgrad(xd[st], W1, W3, W2, dOd, Q)
         dx_shared = dict(zip(st.tolist(), r["dx"]))
-        near_tok |= set(st[r["near"]].tolist())
+        bdx_shared = dict(zip(st.tolist(), r["budget_dx"]))
         if E in wgrad_experts:
-            grads_w[E] = expert_wgrad(xd[st], r["hd"], _fl32(dy[st]) if Q.on else dy[st], r["dA"], r["dB"], Q,
-                                      r["near_h"], dO_exact=True)
+            grads_w[E] = expert_wgrad(xd[st], r["hd"], dys, r["dA"], r["dB"], Q, r["delta_h"], 0.0, r["e_dA"],
+                                      r["e_dB"])
     else:
-        dx_shared = {}
+        dx_shared, bdx_shared = {}, {}
 
     nt = sorted(need_tok)
     dg = np.array([[dy[t] @ out_rows[(t, k)] for k in range(K)] for t in nt]).reshape(len(nt), K)
-    dz_all = gate_grad(np.asarray(s_sel, np.float64)[nt], dg) if nt else np.zeros((0, K))
+    dz_all = gate_grad(s64[nt], dg) if nt else np.zeros((0, K))
+    # dz_k = s_k (1 - s_k) / S * sum_j (delta_kj - g_j) dg_j: a dg range maps through |delta_kj - g_j|
+    bdg = np.array([[bdg_rows[(t, k)] for k in range(K)] for t in nt]).reshape(len(nt), K)
+    if nt:
+        sn, gn = s64[nt], gate[nt]
+        Sn = sn.sum(axis=1, keepdims=True)
+        jac = np.abs(np.eye(K)[None, :, :] - gn[:, None, :])                # [t][k][j]
+        bdz_all = sn * (1.0 - sn) / Sn * np.einsum("tkj,tj->tk", jac, bdg)
+    else:
+        bdz_all = np.zeros((0, K))
     dz_of = dict(zip(nt, dz_all))
     dg_of = dict(zip(nt, dg))
+    bdz_of = dict(zip(nt, bdz_all))
+    bdg_of = dict(zip(nt, bdg))
 
     Wr = np.asarray(Wr, np.float64)
     dx = np.zeros((len(tokens), cfg.d))
+    bdx = np.zeros((len(tokens), cfg.d))
     for i, t in enumerate(tokens.tolist()):
         v = dx_shared[t].copy()
+        b = bdx_shared[t].copy()
         for k in range(K):
             v += dx_rows[(t, k)] + dz_of[t][k] * Wr[idx[t, k]]
+            b += bdx_rows[(t, k)] + bdz_of[t][k] * np.abs(Wr[idx[t, k]])
         dx[i] = v
-    dWr = {}
+        bdx[i] = b
+    dWr, bdWr = {}, {}
     for e in router_experts:
         acc = np.zeros(cfg.d)
+        bacc = np.zeros(cfg.d)
         for t in np.nonzero((idx == e).any(axis=1))[0].tolist():
             k = int(np.nonzero(idx[t] == e)[0][0])
             acc += dz_of[t][k] * x[t]
+            bacc += bdz_of[t][k] * np.abs(x[t])
         dWr[e] = acc
-    return {"dx": dx, "tokens": tokens, "dz": np.array([dz_of[t] for t in tokens.tolist()]).reshape(len(tokens), K),
-            "dg": np.array([dg_of[t] for t in tokens.tolist()]).reshape(len(tokens), K),
+        bdWr[e] = bacc
+    tl = tokens.tolist()
+    return {"dx": dx, "tokens": tokens, "dz": np.array([dz_of[t] for t in tl]).reshape(len(tokens), K),
+            "dg": np.array([dg_of[t] for t in tl]).reshape(len(tokens), K),
             "dW": grads_w, "dWr": dWr,
-            "near": np.array([t in near_tok for t in tokens.tolist()], bool)}
+            "budget": {"dx": bdx, "dz": np.array([bdz_of[t] for t in tl]).reshape(len(tokens), K),
+                       "dg": np.array([bdg_of[t] for t in tl]).reshape(len(tokens), K), "dWr": bdWr}}

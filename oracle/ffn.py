@@ -22,8 +22,11 @@ from . import e4m3
 from .quant import TILE, quant_1x128, quant_128x128
 
 
-def gemm_fp8(qa, sa, qb, sb) -> np.ndarray:
-    """qa u8 [m][k], sa f32 [m][k/128], qb u8 [n][k], sb f32 [n/128][k/128] -> float64 [m][n]."""
+def gemm_fp8(qa, sa, qb, sb, with_abs: bool = False):
+    """qa u8 [m][k], sa f32 [m][k/128], qb u8 [n][k], sb f32 [n/128][k/128] -> float64 [m][n].
+
+    with_abs: also return the sum of |terms| per output (the same sum over |values|), the
+    scale of its evaluation error (bounds.gemm_bound)."""
     A = e4m3.decode(qa)
     B = e4m3.decode(qb)
     m, k = A.shape
@@ -31,12 +34,16 @@ def gemm_fp8(qa, sa, qb, sb) -> np.ndarray:
     sa = np.asarray(sa, np.float64)
     sb = np.asarray(sb, np.float64)
     out = np.zeros((m, n), dtype=np.float64)
+    absout = np.zeros((m, n), dtype=np.float64) if with_abs else None
     for kc in range(k // TILE):
         cols = slice(kc * TILE, (kc + 1) * TILE)
         partial = A[:, cols] @ B[:, cols].T
         col_scale = np.repeat(sb[:, kc], TILE)
-        out += partial * (sa[:, kc][:, None] * col_scale[None, :])
-    return out
+        f = sa[:, kc][:, None] * col_scale[None, :]
+        out += partial * f
+        if with_abs:
+            absout += (np.abs(A[:, cols]) @ np.abs(B[:, cols]).T) * np.abs(f)
+    return (out, absout) if with_abs else out
 
 
 def silu(g):
@@ -63,13 +70,32 @@ class QuantExpert:
         self.q2, self.s2 = quant_128x128(w2, rule)
 
 
-def expert_forward(xq, xs, w: QuantExpert, return_h: bool = False):
-    """xq u8 [m][d], xs f32 [m][d/128] -> float64 [m][d]; h is quantised by the expert's rule."""
-    gate = gemm_fp8(xq, xs, w.q1, w.s1)
-    up = gemm_fp8(xq, xs, w.q3, w.s3)
+def expert_forward(xq, xs, w: QuantExpert, return_h: bool = False, budget: bool = False):
+    """xq u8 [m][d], xs f32 [m][d/128] -> float64 [m][d]; h is quantised by the expert's rule.
+
+    budget: also return, per output element, how far another correct FP32 evaluation may
+    lie from it through the E4M3 decision on h alone (oracle/bounds.py): the gate and up
+    GEMMs' error bounds carried through SiLU, the resulting range of each dequantised h,
+    and that range through |W2|."""
+    if budget:
+        from .bounds import GEMM_C, U, swiglu_h_bound, tile_range
+        from .quant import dequant_128x128
+        gate, ga = gemm_fp8(xq, xs, w.q1, w.s1, with_abs=True)
+        up, ua = gemm_fp8(xq, xs, w.q3, w.s3, with_abs=True)
+        nkc = xq.shape[1] // TILE
+    else:
+        gate = gemm_fp8(xq, xs, w.q1, w.s1)
+        up = gemm_fp8(xq, xs, w.q3, w.s3)
     h = (silu(gate) * up).astype(np.float32)
     hq, hs = quant_1x128(h, w.rule)
     out = gemm_fp8(hq, hs, w.q2, w.s2)
+    if budget:
+        e_h = swiglu_h_bound(gate, up, (nkc + GEMM_C) * U * ga, (nkc + GEMM_C) * U * ua)
+        lo, hi = tile_range(h, e_h, w.rule)
+        hd = e4m3.decode(hq).reshape(h.shape[0], -1, TILE) * np.asarray(hs, np.float64)[:, :, None]
+        hd = hd.reshape(h.shape)
+        delta_h = np.maximum(hi, hd) - np.minimum(lo, hd)
+        return out, delta_h @ np.abs(dequant_128x128(w.q2, w.s2)).T
     if return_h:
         return out, h, hq, hs
     return out

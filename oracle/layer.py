@@ -71,10 +71,13 @@ class Layer:
         c = self.cfg
         return _route.route(x, self.Wr, self.bias, c.G, c.M, c.K, c.gk, self.logit_offset)
 
-    def forward(self, x, tokens=None, idx=None, gate=None, residual=False):
+    def forward(self, x, tokens=None, idx=None, gate=None, residual=False, budget=False):
         """x [T][d] float32 (bf16 values). Returns a dict with y for `tokens` (all by default).
 
-        idx/gate may be given to evaluate the experts for a fixed routing.
+        idx/gate may be given to evaluate the experts for a fixed routing. budget: also
+        "budget", per element of y, how far another correct FP32 evaluation of the layer may
+        lie from y through its E4M3 decisions on h (each expert's, expert_forward) and its
+        gates' error bound (oracle/bounds.py, gate_err), combined with the gates.
         """
         c = self.cfg
         x = np.asarray(x, np.float32)
@@ -85,12 +88,28 @@ class Layer:
         xq, xs = quant_1x128(x[tokens], self.rule)
         n = len(tokens)
         routed = np.zeros((n, c.K, c.d), dtype=np.float64)
+        b_routed = np.zeros((n, c.K, c.d), dtype=np.float64) if budget else None
         sub_idx = np.asarray(idx)[tokens]
         for e in np.unique(sub_idx):
             rows, slots = np.nonzero(sub_idx == e)
-            routed[rows, slots] = expert_forward(xq[rows], xs[rows], self.expert(int(e)))
-        shared = expert_forward(xq, xs, self.expert(c.E))
+            if budget:
+                routed[rows, slots], b_routed[rows, slots] = expert_forward(xq[rows], xs[rows], self.expert(int(e)),
+                                                                            budget=True)
+            else:
+                routed[rows, slots] = expert_forward(xq[rows], xs[rows], self.expert(int(e)))
+        if budget:
+            shared, b_shared = expert_forward(xq, xs, self.expert(c.E), budget=True)
+        else:
+            shared = expert_forward(xq, xs, self.expert(c.E))
         res = x[tokens] if residual else None
-        y = combine(shared, routed, np.asarray(gate)[tokens], res)
-        return {"y": y, "idx": idx, "gate": gate, "info": info, "tokens": tokens,
-                "counts": histogram(idx, c.E), "routed": routed, "shared": shared}
+        g = np.asarray(gate)[tokens]
+        y = combine(shared, routed, g, res)
+        out = {"y": y, "idx": idx, "gate": gate, "info": info, "tokens": tokens,
+               "counts": histogram(idx, c.E), "routed": routed, "shared": shared}
+        if budget:
+            from .bounds import gate_err
+            s = _route.affinity(x[tokens], self.Wr, self.logit_offset)
+            ge = gate_err(np.take_along_axis(s, sub_idx, axis=1))
+            out["budget"] = (b_shared + np.einsum("tk,tkd->td", np.abs(g), b_routed)
+                             + np.einsum("tk,tkd->td", ge, np.abs(routed)))
+        return out

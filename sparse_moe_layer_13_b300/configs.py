@@ -85,4 +85,9 @@ FULLWIDTH_SMALL = MoEConfig("fullwidth_small", T=4096, d=7168, E=32, I=2048, K=8
 # full-width prefill, about 4 GB of device memory for a training step, for profiles of the
 # backward kernels.
 FULLWIDTH_E16 = MoEConfig("fullwidth_e16", T=1024, d=7168, E=16, I=2048, K=8, G=8, M=4, gk=2, seed=6)
-PROFILE_CONFIGS = {c.name: c for c in (FULLWIDTH_SMALL, FULLWIDTH_E16)}
+# The full-width prefill's token shapes (T=16384, d=7168, E=256, K=8, G=8, M=4) with an
+# intermediate size of 128: the router, permutation, quantiser and combine run at exactly
+# their full-width sizes (the fused router included) in about 5 GB of device memory, for
+# DRAM-counter profiles of those calls.
+FULLWIDTH_HBM = MoEConfig("fullwidth_hbm", T=16384, d=7168, E=256, I=128, K=8, G=8, M=4, gk=2, seed=2)
+PROFILE_CONFIGS = {c.name: c for c in (FULLWIDTH_SMALL, FULLWIDTH_E16, FULLWIDTH_HBM)}

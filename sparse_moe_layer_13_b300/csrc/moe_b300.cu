@@ -69,43 +69,37 @@ int num_sms() {
     return sms;
 }
 
-// K split of the router logits GEMM. Each split accumulates at most
-// rtc::kMaxChunksPerSplit chunks in TMEM (the tensor-core accumulation of a
-// long contraction drifts further from a correctly rounded FP32 sum than a
-// short one; the splits are added in FP32 by the selection kernel), and
-// small batches split further so the CTAs cover the SMs. Every split gets
-// at least one chunk.
-int route_ksplit(const moe_config* c) {
+// Router geometry. A CTA accumulates sub-splits of rtc::kMaxChunksPerSplit
+// chunks (the accuracy bound); its K slice is a run of sub-splits. Slices
+// across CTAs exist only to fill the SMs when the token tiles x expert tiles
+// leave them idle (at most rtc::kMaxSlices), each slice non-empty.
+int route_nsub(const moe_config* c) {
+    const int nchunks = 3 * (c->d / rtc::BK);
+    return (nchunks + rtc::kMaxChunksPerSplit - 1) / rtc::kMaxChunksPerSplit;
+}
+
+int route_subs_per_slice(const moe_config* c, int slices) {
+    return (route_nsub(c) + slices - 1) / slices;
+}
+
+int route_slices(const moe_config* c) {
     const int64_t ctas = ceil_div(c->T, rtc::BM) * ceil_div(c->E, rtc::BN_MAX);
-    const int nchunks = 3 * (c->d / rtc::BK);
-    const int ks_acc = (nchunks + rtc::kMaxChunksPerSplit - 1) / rtc::kMaxChunksPerSplit;
-    const int ks_fill = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(16, num_sms() / std::max<int64_t>(ctas, 1))));
-    int ks = std::min(std::max(ks_acc, ks_fill), nchunks);
-    const int per = (nchunks + ks - 1) / ks;
-    return (nchunks + per - 1) / per;
+    const int want = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(rtc::kMaxSlices, num_sms() / std::max<int64_t>(ctas, 1))));
+    const int per = route_subs_per_slice(c, std::min(want, route_nsub(c)));
+    return (route_nsub(c) + per - 1) / per;
 }
 
-// K split of the fused router: the accumulation bound alone (each split at
-// most rtc::kMaxChunksPerSplit chunks), normalised so that every split gets
-// at least one chunk. Equal to route_ksplit whenever the batch alone fills
-// the SMs, so the two paths then add the same partials in the same order.
-int route_ksplit_acc(const moe_config* c) {
-    const int nchunks = 3 * (c->d / rtc::BK);
-    const int ks = (nchunks + rtc::kMaxChunksPerSplit - 1) / rtc::kMaxChunksPerSplit;
-    const int per = (nchunks + ks - 1) / ks;
-    return (nchunks + per - 1) / per;
-}
-
-// The fused router serves E <= 256 when its one CTA per 128-token tile covers
-// at least half the SMs; smaller batches take the K-split path, whose extra
+// The fused router (selection inside the logits kernel) serves E <= 256 when
+// its one CTA per 128-token tile covers at least half the SMs; smaller
+// batches take the sliced logits kernel and the selection kernel, whose extra
 // CTAs fill the GPU.
 bool route_fused_auto(const moe_config* c) {
     return c->E <= rtc::BN_MAX && 2 * ceil_div(c->T, rtc::BM) >= num_sms();
 }
 
-// Workspace layout: [header: split count of the stored router logits, i32,
-// written by the router kernels][router logit partials f32 ksplit*T*E (the
-// fused router stores their sums in the first T*E)][router weight planes bf16
+// Workspace layout: [header: slice count of the stored router logits, i32,
+// written by the router kernels][router logit slice sums f32 slices*T*E (the
+// fused router stores the whole sums in the first T*E)][router weight planes bf16
 // 3*E*d][per-block counts i32 nblk*E][per-block bases i32 nblk*E][offsets
 // scratch i32 E+2][balance chunk sums f32, i32 (T/32)*E each]
 struct WsLayout {
@@ -117,7 +111,7 @@ WsLayout ws_layout(const moe_config* c) {
     const int64_t nblk = ceil_div(c->T, perm::kTokPerBlk);
     w.header = 0;
     w.logits = 256;
-    w.planes = w.logits + align_up(static_cast<size_t>(route_ksplit(c)) * c->T * c->E * sizeof(float), 256);
+    w.planes = w.logits + align_up(static_cast<size_t>(route_slices(c)) * c->T * c->E * sizeof(float), 256);
     w.blk_counts = w.planes + align_up(static_cast<size_t>(3) * c->E * c->d * sizeof(uint16_t), 256);
     w.blk_base = w.blk_counts + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
     w.offsets = w.blk_base + align_up(static_cast<size_t>(nblk) * c->E * sizeof(int32_t), 256);
@@ -211,37 +205,38 @@ void launch_select(const moe_config* c, const float* z, int ks, const float* off
     else launch_select_e<32>(c, z, ks, off, bias, idx, gate, grid, smem, st);
 }
 
-template <int EPL, int MAXGK>
-moe_status launch_fused_t(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, int ks,
+template <bool SELECT, int EPL, int MAXGK>
+moe_status launch_route_t(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, int slices,
                           const float* off, const float* bias, int32_t* idx, float* gate, float* z, int* splits,
                           cudaStream_t st) {
     static std::atomic<uint64_t> attr_done{0};
-    if (smem_attr(reinterpret_cast<const void*>(rtc::fused_kernel<EPL, MAXGK>), rtc::F_SMEM_BYTES, attr_done) !=
-        MOE_OK)
+    if (smem_attr(reinterpret_cast<const void*>(rtc::route_kernel<SELECT, EPL, MAXGK>), rtc::F_SMEM_BYTES,
+                  attr_done) != MOE_OK)
         return MOE_ERR_CUDA;
-    rtc::FParams fp{c->T, c->d, c->E, ks, c->G, c->M, c->K, c->gk, off, bias, idx, gate, z, splits};
-    rtc::fused_kernel<EPL, MAXGK><<<static_cast<unsigned>(ceil_div(c->T, rtc::BM)), rtc::F_THREADS,
-                                    rtc::F_SMEM_BYTES, st>>>(tx, tw, fp);
+    rtc::FParams fp{c->T, c->d, c->E, c->G, c->M, c->K, c->gk, route_subs_per_slice(c, slices),
+                    off, bias, idx, gate, z, splits};
+    const dim3 grid(static_cast<unsigned>(ceil_div(c->T, rtc::BM)),
+                    SELECT ? 1u : static_cast<unsigned>(ceil_div(c->E, rtc::BN_MAX)), static_cast<unsigned>(slices));
+    rtc::route_kernel<SELECT, EPL, MAXGK><<<grid, rtc::F_THREADS, rtc::F_SMEM_BYTES, st>>>(tx, tw, fp);
     return launch_status();
 }
 
 template <int EPL>
-moe_status launch_fused_e(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, int ks,
-                          const float* off, const float* bias, int32_t* idx, float* gate, float* z, int* splits,
-                          cudaStream_t st) {
-    if (c->gk <= 2) return launch_fused_t<EPL, 2>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
-    if (c->gk <= 4) return launch_fused_t<EPL, 4>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
-    return launch_fused_t<EPL, route::kMaxGK>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
+moe_status launch_fused_e(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, const float* off,
+                          const float* bias, int32_t* idx, float* gate, float* z, int* splits, cudaStream_t st) {
+    if (c->gk <= 2) return launch_route_t<true, EPL, 2>(c, tx, tw, 1, off, bias, idx, gate, z, splits, st);
+    if (c->gk <= 4) return launch_route_t<true, EPL, 4>(c, tx, tw, 1, off, bias, idx, gate, z, splits, st);
+    return launch_route_t<true, EPL, route::kMaxGK>(c, tx, tw, 1, off, bias, idx, gate, z, splits, st);
 }
 
-// The fused router (E <= 256: at most 8 experts per lane).
-moe_status launch_fused(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, int ks, const float* off,
+// The fused router: one K slice, selection in the kernel (E <= 256: at most 8 experts per lane).
+moe_status launch_fused(const moe_config* c, const CUtensorMap& tx, const CUtensorMap& tw, const float* off,
                         const float* bias, int32_t* idx, float* gate, float* z, int* splits, cudaStream_t st) {
     const int epl = (c->E + 31) / 32;
-    if (epl <= 1) return launch_fused_e<1>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
-    if (epl <= 2) return launch_fused_e<2>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
-    if (epl <= 4) return launch_fused_e<4>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
-    return launch_fused_e<8>(c, tx, tw, ks, off, bias, idx, gate, z, splits, st);
+    if (epl <= 1) return launch_fused_e<1>(c, tx, tw, off, bias, idx, gate, z, splits, st);
+    if (epl <= 2) return launch_fused_e<2>(c, tx, tw, off, bias, idx, gate, z, splits, st);
+    if (epl <= 4) return launch_fused_e<4>(c, tx, tw, off, bias, idx, gate, z, splits, st);
+    return launch_fused_e<8>(c, tx, tw, off, bias, idx, gate, z, splits, st);
 }
 
 // to: the FP32 output's tensor map for the all-FP32 epilogues (unused by the others)
@@ -464,19 +459,12 @@ moe_status moe_route_planes(const moe_config* cfg, const uint16_t* x, const uint
                        static_cast<uint32_t>(bn)))
         return MOE_ERR_CUDA;
     if (fused) {
-        if (launch_fused(cfg, tx, tw, route_ksplit_acc(cfg), logit_offset, bias, topk_idx, topk_gate, z, splits, st) !=
-            MOE_OK)
+        if (launch_fused(cfg, tx, tw, logit_offset, bias, topk_idx, topk_gate, z, splits, st) != MOE_OK)
             return MOE_ERR_CUDA;
     } else {
-        const int ks = route_ksplit(cfg);
-        static std::atomic<uint64_t> attr_done{0};
-        if (smem_attr(reinterpret_cast<const void*>(rtc::logits_kernel), rtc::SMEM_BYTES, attr_done) != MOE_OK)
+        const int ks = route_slices(cfg);
+        if (launch_route_t<false, 1, 2>(cfg, tx, tw, ks, nullptr, nullptr, nullptr, nullptr, z, splits, st) != MOE_OK)
             return MOE_ERR_CUDA;
-        const dim3 lg(static_cast<unsigned>(ceil_div(cfg->T, rtc::BM)),
-                      static_cast<unsigned>(ceil_div(cfg->E, rtc::BN_MAX)), static_cast<unsigned>(ks));
-        rtc::Params rp{cfg->T, cfg->d, cfg->E, bn, ks, z, splits};
-        rtc::logits_kernel<<<lg, rtc::NUM_THREADS, rtc::SMEM_BYTES, st>>>(tx, tw, rp);
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
         const size_t sel_smem = static_cast<size_t>(route::kSelWarps) * 2 * cfg->E * sizeof(float);
         const int sel_grid = static_cast<int>(std::min<int64_t>(ceil_div(cfg->T, route::kSelWarps), 65535));
         launch_select(cfg, z, ks, logit_offset, bias, topk_idx, topk_gate, sel_grid, sel_smem, st);

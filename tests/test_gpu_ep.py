@@ -99,8 +99,9 @@ def _ep_case(cfg, R, check_oracle=True):
         tie = near_tie(info)
         tokens = np.nonzero(~tie)[0]
         ex = oracle_experts(cfg, set(ref_idx[tokens].ravel().tolist()) | {cfg.E})
-        ref = Layer(cfg, Wr, b0, None, experts=ex).forward(xn, tokens=tokens, idx=ref_idx, gate=ref_gate)
-        assert_y_close(ye[tokens], ref["y"])
+        ref = Layer(cfg, Wr, b0, None, experts=ex).forward(xn, tokens=tokens, idx=ref_idx, gate=ref_gate,
+                                                           budget=True)
+        assert_y_close(ye[tokens], ref["y"], ref["budget"])
     return states
 
 

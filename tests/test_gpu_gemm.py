@@ -246,3 +246,40 @@ def test_gemm_reports_corrupt_offsets():
     binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, binding.MOE_EPI_BF16, out)
     with pytest.raises(binding.MoeError):
         binding.check_device_status()
+
+
+@gpu
+@pytest.mark.parametrize("K", [2048, 7168])
+def test_gemm_f32_within_evaluation_bound(K):
+    """Pins the evaluation bound the oracle's gradient and output budgets rest on
+    (oracle/bounds.py, gemm_bound): every FP32 output of the grouped GEMM lies within
+    (nkc + GEMM_C) * 2^-24 * sum|terms| of the exact chunk-promoted sum, on operands quantised
+    from Gaussian values as the layer's are (1x128 activations, 128x128 weight blocks)."""
+    require_gpu()
+    from oracle.bounds import GEMM_C, U
+    from oracle.quant import quant_128x128
+    from sparse_moe_layer_13_b300 import binding
+    rng = np.random.default_rng(K)
+    sizes = [300, 0, 129, 512]
+    N = 512
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    rows = int(offsets[-1])
+    A, sa = quant_1x128(rng.standard_normal((rows, K)).astype(np.float32))
+    Bq, sb = zip(*(quant_128x128((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
+                   for _ in sizes))
+    B, sb = np.stack(Bq), np.stack(sb)
+    o_d, A_d, sa_d, B_d, sb_d = _cuda(offsets, A, sa, B, sb)
+    out, _ = binding.grouped_gemm_fp8(o_d, A_d, sa_d, B_d, sb_d, binding.MOE_EPI_F32)
+    binding.check_device_status()
+    got = to_np(out).astype(np.float64)
+    worst = 0.0
+    for g in range(len(sizes)):
+        r0, r1 = offsets[g], offsets[g + 1]
+        if r1 == r0:
+            continue
+        exact, absum = gemm_fp8(A[r0:r1], sa[r0:r1], B[g], sb[g], with_abs=True)
+        bound = (K // 128 + GEMM_C) * U * absum
+        ratio = np.abs(got[r0:r1] - exact) / bound
+        worst = max(worst, float(ratio.max()))
+        assert (ratio <= 1.0).all(), f"group {g}: {int((ratio > 1).sum())} outputs beyond the bound"
+    print(f"[bound] K={K}: worst |error| / ((nkc + {GEMM_C}) u sum|terms|) = {worst:.3f}")

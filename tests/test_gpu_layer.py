@@ -32,9 +32,9 @@ def _layer_case(cfg, n_sample=None, residual=False, seed=0, rule="fp32"):
     needed = set(ref_idx[tokens].ravel().tolist()) | {cfg.E}
     ex = oracle_experts(cfg, needed, rule=rule)
     ref = Layer(cfg, Wr, b0, None, experts=ex, rule=rule).forward(xn, tokens=tokens, idx=ref_idx, gate=ref_gate,
-                                                                  residual=residual)
+                                                                  residual=residual, budget=True)
     keep = ~tie[tokens]
-    rel, mx = assert_y_close(y[tokens][keep], ref["y"][keep])
+    rel, mx = assert_y_close(y[tokens][keep], ref["y"][keep], ref["budget"][keep])
     check_load_and_bias(cfg, to_np(layer.idx), to_np(layer.counts), ref_idx, tie, b0, to_np(layer.bias))
     return rel, mx, layer
 

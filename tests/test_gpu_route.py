@@ -101,8 +101,8 @@ def _stored_logits(cfg, ws):
 @gpu
 @pytest.mark.parametrize("T", [16384, 16384 + 37])
 def test_route_fused_equals_split_path_bit_for_bit(T):
-    """At full width both router paths use 14 K splits, so the fused kernel's in-register
-    sums must equal the split path's stored partials summed in order: identical logits,
+    """At full width the token tiles alone fill the SMs, so the sliced path runs one K slice
+    per tile: its stored sums must equal the fused kernel's bit for bit, and so must the
     choice, gates and loads."""
     require_gpu()
     from sparse_moe_layer_13_b300 import binding, inputs
@@ -119,7 +119,7 @@ def test_route_fused_equals_split_path_bit_for_bit(T):
         idx, gate, counts = binding.route_planes(cfg, x, planes, bias, workspace=ws, want_counts=True, path=path)
         binding.check_device_status()
         out[path] = (idx, gate, counts, *_stored_logits(cfg, ws))
-    assert out["split"][3] == 14 and out["fused"][3] == 1
+    assert out["split"][3] == 1 and out["fused"][3] == 1
     assert np.array_equal(out["split"][4], out["fused"][4])
     for i in range(3):
         assert torch.equal(out["split"][i], out["fused"][i])
@@ -169,3 +169,34 @@ def test_route_planes_rejects_fused_beyond_256_experts():
     with pytest.raises(binding.MoeError) as e:
         binding.route_planes(c, x, binding.router_planes(Wr), torch.zeros(c.E, device="cuda"), path="fused")
     assert e.value.code == 2
+
+
+@gpu
+def test_route_experts_beyond_one_tile_ragged():
+    """E = 320: two expert tiles of the sliced logits kernel, the last one 64 wide (its
+    weight box still carries 256 rows), with a ragged token tail."""
+    require_gpu()
+    _run(MoEConfig("e320", T=300, d=256, E=320, I=128, K=8, G=4, M=2, gk=2, seed=13, bias="uniform"))
+
+
+@gpu
+@pytest.mark.parametrize("name", ["full", "decode"])
+def test_router_logits_within_stated_bound(name):
+    """Pins the router bound the oracle's gate error rests on (oracle/bounds.py,
+    ROUTER_LOGIT_ERR): the logits the router leaves in the workspace (fused path at full
+    width, sliced path for the decode batch) lie within it of x . Wr in FP64."""
+    require_gpu()
+    from oracle.bounds import ROUTER_LOGIT_ERR
+    from sparse_moe_layer_13_b300 import binding, inputs
+    cfg = CONFIGS[name]
+    x = inputs.gen_x(cfg, "cuda")
+    Wr = inputs.gen_router(cfg, "cuda")
+    ws = torch.zeros(binding.workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    binding.route(cfg, x, Wr, inputs.gen_bias(cfg, "cuda"), None, ws)
+    binding.check_device_status()
+    _, z = _stored_logits(cfg, ws)
+    tok = np.arange(0, cfg.T, 7)
+    exact = to_np(x)[tok].astype(np.float64) @ to_np(Wr).astype(np.float64).T
+    err = np.abs(z[tok].astype(np.float64) - exact)
+    print(f"[router] {name}: max |logit - exact| {err.max():.3e}, mean {err.mean():.3e} (bound {ROUTER_LOGIT_ERR:g})")
+    assert err.max() <= ROUTER_LOGIT_ERR

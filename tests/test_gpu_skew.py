@@ -63,6 +63,7 @@ def test_skew_balancing_loop_and_forward_match_oracle():
     rest = rng.choice(np.setdiff1d(np.nonzero(~tie)[0], hot_tok), 48, replace=False)
     tokens = np.sort(np.concatenate([hot_tok, rest]))
     ex = oracle_experts(cfg, set(r_idx[tokens].ravel().tolist()) | {cfg.E})
-    ref = Layer(cfg, Wr, b0, None, logit_offset=offn, experts=ex).forward(xn, tokens=tokens, idx=r_idx, gate=r_gate)
-    assert_y_close(y[tokens], ref["y"])
+    ref = Layer(cfg, Wr, b0, None, logit_offset=offn, experts=ex).forward(xn, tokens=tokens, idx=r_idx, gate=r_gate,
+                                                                          budget=True)
+    assert_y_close(y[tokens], ref["y"], ref["budget"])
     torch.cuda.synchronize()

@@ -15,8 +15,9 @@ import numpy as np
 import pytest
 
 from oracle import e4m3
-from oracle.backward import (Quantiser, dequant_128x1_grouped, gate_grad, gemm_fp8_wgrad, layer_backward,
-                             near_midpoint, quant_128x1_grouped, segment_starts, swiglu_grad)
+from oracle.bounds import GEMM_C, U
+from oracle.backward import (Quantiser, dequant_128x1_grouped, gate_grad, gemm_bound, gemm_fp8_wgrad,
+                             layer_backward, quant_128x1_grouped, segment_starts, swiglu_grad)
 
 
 class _Cfg:
@@ -189,20 +190,104 @@ def test_quantised_gradients_near_exact():
             assert rel(quant["dW"][e][j], exact["dW"][e][j]) < 0.08
 
 
-def test_near_midpoint():
-    # E4M3 grid around 1: spacing 1/8 in [1, 2), 1/16 in [0.5, 1); 448 is the top value
-    assert near_midpoint(np.array([1.0625]))[0]                     # the midpoint of 1 and 1.125
-    assert near_midpoint(np.array([1.0625 * (1 + 1e-5)]))[0]
-    assert not near_midpoint(np.array([1.0625 * (1 + 1e-4)]))[0]
-    assert not near_midpoint(np.array([1.0, 1.125, 0.0, 448.0, 40.0])).any()
-    assert near_midpoint(np.array([0.53125]))[0]                    # midpoint of 0.5 and 0.5625
-    assert near_midpoint(np.array([2.0 ** -10]))[0]                 # subnormal grid, spacing 2^-9
-    # a value on a midpoint is exactly where encode's tie rule decides: flipping the
-    # last FP32 bit either way moves the code by one
-    for v in (1.0625, 0.53125, 42.0, -304.0):
-        up = e4m3.encode(np.nextafter(np.float32(v), np.float32(np.inf)))
-        dn = e4m3.encode(np.nextafter(np.float32(v), np.float32(-np.inf)))
-        assert up != dn and near_midpoint(np.array([v]))[0]
+def test_quantiser_range_at_and_away_from_rounding_midpoints():
+    """The range of dequantised values under an input error bound: zero for zero error; one
+    whole code step for a value on a rounding midpoint of the E4M3 grid (the neighbouring codes
+    are both reachable); only the scale's own relative variation for a value far from every
+    boundary. In a tile whose amax is 448 * 1 (scale 1), 1.0625 sits between codes 1 and
+    1.125, 0.53125 between 0.5 and 0.5625, 2^-10 on the subnormal grid (spacing 2^-9)."""
+    Q = Quantiser("fp32")
+    row = np.zeros((1, 128), np.float32)
+    row[0, 0] = 448.0                                   # amax 448: scale exactly 1
+    vals = [1.0625, 0.53125, 2.0 ** -10, 1.0, 40.0]
+    row[0, 1:1 + len(vals)] = vals
+    Q.rows(row, 0.0)
+    assert not Q.delta.any()
+    err = np.zeros((1, 128))
+    err[0, 1:1 + len(vals)] = 1e-6
+    Q.rows(row, err)
+    d = Q.delta[0, 1:1 + len(vals)]
+    assert d[0] == 0.125 and d[1] == 0.0625 and d[2] == 2.0 ** -9     # both neighbours reachable
+    assert d[3] == 0.0 and d[4] == 0.0                                 # exact grid points, amax certain
+    # the amax's own error moves the scale: every value then ranges with it (relative ~ err/amax)
+    err[0, 0] = 448 * 1e-4
+    Q.rows(row, err)
+    assert 0 < Q.delta[0, 4] < 40.0 * 3e-4
+
+
+def test_gemm_bound_covers_float32_chunked_evaluation():
+    """gemm_bound against a float32 evaluation written out the way a chunk-promoted GEMM
+    works (float32 chunk partial sums, float32 promotion per chunk): the float32 result lies
+    within the bound of the exact product, and the bound is not vacuous (a few per cent of
+    it is used on some element)."""
+    rng = np.random.default_rng(8)
+    m, k, n = 16, 1024, 24
+    A = (rng.standard_normal((m, k)) * np.exp(rng.uniform(-3, 3, (m, k)))).astype(np.float32).astype(np.float64)
+    B = rng.standard_normal((k, n)).astype(np.float32).astype(np.float64)
+    exact = A @ B
+    acc = np.zeros((m, n), np.float32)
+    for c in range(k // 128):
+        part = np.zeros((m, n), np.float32)
+        for j in range(c * 128, (c + 1) * 128):
+            part = (part + (A[:, j:j + 1] * B[j:j + 1, :]).astype(np.float32)).astype(np.float32)
+        acc = (acc + part).astype(np.float32)
+    bound = gemm_bound(A, B, k // 128)
+    err = np.abs(acc.astype(np.float64) - exact)
+    assert (err <= bound).all()
+    assert (err / bound).max() > 0.01
+    assert np.allclose(bound, (k // 128 + GEMM_C) * U * (np.abs(A) @ np.abs(B)))
+
+
+def _planted_case(plant):
+    """Weight gradients of a small layer, with one 128x1 code of dA moved by a step when
+    `plant`, on an element whose range is far below a code step (only its tile scale may vary:
+    no correct evaluation could change its code)."""
+    import oracle.backward as bw
+    rng = np.random.default_rng(9)
+    T, d, E, I, K = 64, 256, 2, 128, 1
+    cfg = _Cfg(T, d, E, I, K)
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    dy = rng.standard_normal((T, d)).astype(np.float32)
+    Wr = rng.standard_normal((E, d)) / np.sqrt(d)
+    W = {e: tuple(rng.standard_normal(sh) / np.sqrt(d) for sh in ((I, d), (I, d), (d, I))) for e in range(E + 1)}
+    idx = np.zeros((T, K), np.int32)
+    s_sel = np.full((T, K), 0.5)
+    real_tokens = bw.Quantiser.tokens
+    picked = {}
+
+    def tokens(self, v, err=0.0):
+        out = real_tokens(self, v, err)
+        if plant and v.shape == (T, I) and "done" not in picked:
+            certain = np.argwhere((self.delta < 1e-3 * np.abs(out)) & (np.abs(out) > 0))
+            t, i = certain[len(certain) // 2]
+            picked.update(done=True, at=(t, i))
+            out = out.copy()
+            out[t, i] *= 1.0625 if abs(out[t, i]) < 0.5 * np.abs(out[:, i]).max() else 0.9375
+        return out
+
+    bw.Quantiser.tokens = tokens
+    try:
+        r = layer_backward(cfg, x, dy, Wr, idx, s_sel, lambda e: W[e], wgrad_experts=[0], Q=Quantiser())
+    finally:
+        bw.Quantiser.tokens = real_tokens
+    return r["dW"][0]
+
+
+def test_budget_check_catches_a_flip_outside_the_ranges():
+    """The weight-gradient check a device result must meet, element by element: within
+    budget + base (the quantisation ranges' effect plus the contraction's own FP32 bound) of
+    the oracle. The oracle's own result passes it; the same computation with one dA code
+    moved by a step, on an element whose range is only its scale's variation (no correct
+    evaluation could change that code), fails it."""
+    clean = _planted_case(False)
+    bad = _planted_case(True)
+    dW1 = clean[0]
+    allow = clean[3]["dW1"] + clean[3]["base"]["dW1"]
+    assert (np.abs(clean[0] - dW1) <= allow).all()
+    assert (np.abs(bad[0] - dW1) > allow).any()
+    # the allowance is a small part of the gradient as a whole (it cannot hide a systematic
+    # error); a single row may carry more where an uncertain code sits at its column's maximum
+    assert np.linalg.norm(allow) <= 2e-2 * np.linalg.norm(dW1)
 
 
 def test_scaled_rows_reduces_to_plain_quantisation():
