@@ -226,8 +226,8 @@ def expert_dgrad(xd, W1, W3, W2, dOd, Q: Quantiser, dOd_delta=None, dOd_row_rel=
     h = silu * b
     d, I = xd.shape[1], W1.shape[0]
     if Q.on:
-        e_a = gemm_bound(xd, W1.T, d // TILE)
-        e_b = gemm_bound(xd, W3.T, d // TILE)
+        e_a = gemm_bound(xd, W1.T)
+        e_b = gemm_bound(xd, W3.T)
         e_h = swiglu_h_bound(a, b, e_a, e_b)
     else:
         e_a = e_b = e_h = np.zeros_like(a)
@@ -235,9 +235,8 @@ def expert_dgrad(xd, W1, W3, W2, dOd, Q: Quantiser, dOd_delta=None, dOd_row_rel=
     delta_h = Q.delta
     out = hd @ W2.T
     dh = dOd @ W2
-    Ip = (I + 255) // 256 * 256                     # the dh GEMM runs over I padded to 256
     if Q.on:
-        e_dh = gemm_bound(dOd, W2, Ip // TILE)
+        e_dh = gemm_bound(dOd, W2)
         if dOd_row_rel is not None:
             e_dh = e_dh + dOd_row_rel[:, None] * np.abs(dh)
         elif dOd_delta is not None:
@@ -278,9 +277,8 @@ def expert_wgrad(xd, hd, dO, dA, dB, Q: Quantiser, delta_h=None, e_dO=0.0, e_dA=
                "dW2": rO.T @ np.abs(ht) + np.abs(dOt).T @ rh}
     if Q.on:
         # the contraction's own FP32 evaluation over the expert's 128-token chunks
-        nkc = (xd.shape[0] + TILE - 1) // TILE
-        budgets["base"] = {"dW1": gemm_bound(dAt.T, xt, nkc), "dW3": gemm_bound(dBt.T, xt, nkc),
-                           "dW2": gemm_bound(dOt.T, ht, nkc)}
+        budgets["base"] = {"dW1": gemm_bound(dAt.T, xt), "dW3": gemm_bound(dBt.T, xt),
+                           "dW2": gemm_bound(dOt.T, ht)}
     return dAt.T @ xt, dBt.T @ xt, dOt.T @ ht, budgets
 
 

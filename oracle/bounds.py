@@ -11,10 +11,14 @@ dequantised operand then differs by a whole code step. The pages give no error
 bound, so the bounds here are derived from the arithmetic:
 
 * gemm_bound: an FP8 GEMM promoted per 128-element chunk, evaluated in FP32,
-  lies within (nkc + GEMM_C) * u * sum|terms| of the exact sum (u = 2^-24:
-  first-order, one rounding of the running sum per chunk and a fixed number
-  for each chunk's own sum, scale product and fused multiply-add). GEMM_C is
-  pinned against the device's FP32-output GEMMs by a GPU test.
+  lies within u * (CHUNK_ROUNDINGS * sum|terms| + sum over chunks of
+  (|f P| + |acc|)) of the exact sum (u = 2^-24, first order). Inside a chunk
+  the tensor core adds four K=32 steps of exact E4M3 products into an FP32
+  accumulator, each rounding once on a partial sum no larger than the chunk's
+  sum of |terms|; the promotion rounds the chunk's scale product (|f P|) and
+  its fused multiply-add into the running sum (|acc| after the chunk), both
+  evaluated from the exact partial sums. Pinned against the device's
+  FP32-output GEMMs by GPU tests.
 * elementwise FP32 chains (SiLU and its gradient) add a few ulps (ARITH_ULPS;
   FAST_ULPS for the forward's fast exponential and division), and first-order
   sensitivities carry input bounds through them.
@@ -36,15 +40,26 @@ from . import e4m3
 from .quant import TILE, dequant_1x128, quant_1x128, tile_scale
 
 U = 2.0 ** -24           # unit roundoff of FP32 (round to nearest)
-GEMM_C = 10              # fixed part of gemm_bound's count of roundings
+CHUNK_ROUNDINGS = 4      # K=32 tensor-core steps per 128-element chunk, one rounding each
 ARITH_ULPS = 8           # an elementwise FP32 chain with exp and division (SiLU, its gradient)
 FAST_ULPS = 16           # the same with the fast exponential and division
 ROUTER_LOGIT_ERR = 1e-5  # |router logit - exact| of a correct FP32 router at these widths
 
 
-def gemm_bound(A, B, nkc: int) -> np.ndarray:
-    """(nkc + GEMM_C) * u * (|A| @ |B|): bound on |FP32 chunk-promoted evaluation - exact| of A @ B."""
-    return (nkc + GEMM_C) * U * (np.abs(A) @ np.abs(B))
+def gemm_bound(A, B) -> np.ndarray:
+    """Bound on |FP32 chunk-promoted evaluation - exact| of A @ B for dequantised operands
+    (the chunk scales folded into the values), contraction in chunks of 128:
+    u * (CHUNK_ROUNDINGS * (|A| @ |B|) + sum_i |P_i| + sum_i |acc_i|), P_i chunk i's partial
+    product, acc_i the running sum after it."""
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    acc = np.zeros((A.shape[0], B.shape[1]))
+    run = np.zeros_like(acc)
+    for c in range(0, A.shape[1], TILE):
+        p = A[:, c:c + TILE] @ B[c:c + TILE]
+        acc += p
+        run += np.abs(p) + np.abs(acc)
+    return U * (CHUNK_ROUNDINGS * (np.abs(A) @ np.abs(B)) + run)
 
 
 def gate_err(s_sel) -> np.ndarray:

@@ -22,11 +22,11 @@ from . import e4m3
 from .quant import TILE, quant_1x128, quant_128x128
 
 
-def gemm_fp8(qa, sa, qb, sb, with_abs: bool = False):
+def gemm_fp8(qa, sa, qb, sb, with_bound: bool = False):
     """qa u8 [m][k], sa f32 [m][k/128], qb u8 [n][k], sb f32 [n/128][k/128] -> float64 [m][n].
 
-    with_abs: also return the sum of |terms| per output (the same sum over |values|), the
-    scale of its evaluation error (bounds.gemm_bound)."""
+    with_bound: also return, per output, the bound on an FP32 evaluation's error
+    (oracle/bounds.py, gemm_bound), from the same chunk partial sums."""
     A = e4m3.decode(qa)
     B = e4m3.decode(qb)
     m, k = A.shape
@@ -34,16 +34,20 @@ def gemm_fp8(qa, sa, qb, sb, with_abs: bool = False):
     sa = np.asarray(sa, np.float64)
     sb = np.asarray(sb, np.float64)
     out = np.zeros((m, n), dtype=np.float64)
-    absout = np.zeros((m, n), dtype=np.float64) if with_abs else None
+    if with_bound:
+        from .bounds import CHUNK_ROUNDINGS, U
+        absum = np.zeros((m, n), dtype=np.float64)
+        run = np.zeros((m, n), dtype=np.float64)
     for kc in range(k // TILE):
         cols = slice(kc * TILE, (kc + 1) * TILE)
         partial = A[:, cols] @ B[:, cols].T
         col_scale = np.repeat(sb[:, kc], TILE)
         f = sa[:, kc][:, None] * col_scale[None, :]
         out += partial * f
-        if with_abs:
-            absout += (np.abs(A[:, cols]) @ np.abs(B[:, cols]).T) * np.abs(f)
-    return (out, absout) if with_abs else out
+        if with_bound:
+            absum += (np.abs(A[:, cols]) @ np.abs(B[:, cols]).T) * np.abs(f)
+            run += np.abs(partial * f) + np.abs(out)
+    return (out, U * (CHUNK_ROUNDINGS * absum + run)) if with_bound else out
 
 
 def silu(g):
@@ -78,11 +82,10 @@ def expert_forward(xq, xs, w: QuantExpert, return_h: bool = False, budget: bool 
     GEMMs' error bounds carried through SiLU, the resulting range of each dequantised h,
     and that range through |W2|."""
     if budget:
-        from .bounds import GEMM_C, U, swiglu_h_bound, tile_range
+        from .bounds import swiglu_h_bound, tile_range
         from .quant import dequant_128x128
-        gate, ga = gemm_fp8(xq, xs, w.q1, w.s1, with_abs=True)
-        up, ua = gemm_fp8(xq, xs, w.q3, w.s3, with_abs=True)
-        nkc = xq.shape[1] // TILE
+        gate, e_gate = gemm_fp8(xq, xs, w.q1, w.s1, with_bound=True)
+        up, e_up = gemm_fp8(xq, xs, w.q3, w.s3, with_bound=True)
     else:
         gate = gemm_fp8(xq, xs, w.q1, w.s1)
         up = gemm_fp8(xq, xs, w.q3, w.s3)
@@ -90,7 +93,7 @@ def expert_forward(xq, xs, w: QuantExpert, return_h: bool = False, budget: bool 
     hq, hs = quant_1x128(h, w.rule)
     out = gemm_fp8(hq, hs, w.q2, w.s2)
     if budget:
-        e_h = swiglu_h_bound(gate, up, (nkc + GEMM_C) * U * ga, (nkc + GEMM_C) * U * ua)
+        e_h = swiglu_h_bound(gate, up, e_gate, e_up)
         lo, hi = tile_range(h, e_h, w.rule)
         hd = e4m3.decode(hq).reshape(h.shape[0], -1, TILE) * np.asarray(hs, np.float64)[:, :, None]
         hd = hd.reshape(h.shape)

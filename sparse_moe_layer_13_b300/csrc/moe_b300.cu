@@ -509,8 +509,8 @@ moe_status moe_quant_fp8_1x128_rule(const uint16_t* x, int64_t rows, int64_t col
     if (cols % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0 || cols == 0) return MOE_OK;
     const int64_t tiles = rows * (cols / 128);
-    // 8 warps per CTA, two tiles per warp step, two steps in flight per thread
-    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 32), static_cast<int64_t>(num_sms()) * 16));
+    // 8 warps per CTA, four tiles per warp step, two steps in flight per thread
+    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 64), static_cast<int64_t>(num_sms()) * 16));
     if (rule == MOE_SCALE_POW2)
         quant_1x128_kernel<false, true><<<grid, 256, 0, as_stream(stream)>>>(x, rows, cols, ld, q, scale, nullptr, 0);
     else
@@ -530,7 +530,7 @@ moe_status moe_quant_fp8_1x128_scatter_rule(const moe_config* cfg, const uint16_
     if (!aligned16(x) || !aligned16(xq_perm)) return MOE_ERR_INVALID_ARG;
     if (rule != MOE_SCALE_FP32 && rule != MOE_SCALE_POW2) return MOE_ERR_INVALID_ARG;
     const int64_t tiles = static_cast<int64_t>(cfg->T) * (cfg->d / 128);
-    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 32), static_cast<int64_t>(num_sms()) * 16));
+    const int grid = static_cast<int>(std::min<int64_t>(ceil_div(tiles, 64), static_cast<int64_t>(num_sms()) * 16));
     if (rule == MOE_SCALE_POW2)
         quant_1x128_kernel<true, true><<<grid, 256, 0, as_stream(stream)>>>(x, cfg->T, cfg->d, cfg->d, xq_perm,
                                                                           xs_perm, row_of, cfg->K);

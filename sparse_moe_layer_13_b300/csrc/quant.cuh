@@ -9,15 +9,15 @@
 
 namespace moe {
 
-// Half a warp per 1x128 tile: 8 bf16 values per lane (16-byte loads), amax
-// by shuffles inside the half warp, 8 E4M3 codes per lane (8-byte stores);
-// each warp step covers two tiles and a thread keeps two steps in flight.
-// Grid-stride over tile pairs, so any grid size is valid.
+// Eight lanes per 1x128 tile: 16 bf16 values per lane (two 16-byte loads), amax
+// by shuffles inside the eight lanes, 16 E4M3 codes per lane (one 16-byte
+// store); each warp step covers four tiles and a thread keeps two steps in
+// flight. Grid-stride over groups of four tiles, so any grid size is valid.
 // SCATTER: row r of x is token r of a routed batch; its codes and scale go
 // to the K grouped rows row_of[r][0..K) and to the shared-expert row
-// rows*K + r of q / scale instead of to row r (K <= 16: lane k of the half
-// warp loads row_of[r][k]). A grouped row outside [0, rows*K) is reported
-// and not written.
+// rows*K + r of q / scale instead of to row r (K <= 16: lane j of the eight
+// loads row_of[r][j] and row_of[r][8 + j]). A grouped row outside
+// [0, rows*K) is reported and not written.
 template <bool SCATTER, bool POW2>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                           int64_t cols, int64_t ld, uint8_t* __restrict__ q,
@@ -25,55 +25,72 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ row_of, int K) {
     const int64_t tiles_per_row = cols / 128;
     const int64_t ntiles = rows * tiles_per_row;
-    const int64_t npairs = (ntiles + 1) / 2;
+    const int64_t nquads = (ntiles + 3) / 4;
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const uint32_t lane = lane_id();
-    const uint32_t sub = lane & 15;
-    for (int64_t p0 = warp; p0 < npairs; p0 += 2 * nwarps) {
-        uint4 w[2];
+    const uint32_t sub = lane & 7;
+    const uint32_t base = lane & 24;                       // first lane of this tile's eight
+    for (int64_t p0 = warp; p0 < nquads; p0 += 2 * nwarps) {
+        uint4 w[2][2];
         int64_t tile[2];
         bool live[2];
-        int dst[2] = {0, 0};
+        int dst[2][2] = {{0, 0}, {0, 0}};
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            tile[u] = 2 * (p0 + u * nwarps) + (lane >> 4);
-            live[u] = (p0 + u * nwarps) < npairs && tile[u] < ntiles;
-            w[u] = make_uint4(0, 0, 0, 0);
+            tile[u] = 4 * (p0 + u * nwarps) + (lane >> 3);
+            live[u] = (p0 + u * nwarps) < nquads && tile[u] < ntiles;
+            w[u][0] = w[u][1] = make_uint4(0, 0, 0, 0);
             if (live[u]) {
                 const int64_t r = tile[u] / tiles_per_row, c = tile[u] - r * tiles_per_row;
-                w[u] = __ldg(reinterpret_cast<const uint4*>(x + r * ld + c * 128) + sub);
-                if (SCATTER && static_cast<int>(sub) < K) dst[u] = __ldg(row_of + r * K + sub);
+                const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + c * 128) + 2 * sub;
+                w[u][0] = __ldg(src);
+                w[u][1] = __ldg(src + 1);
+                if (SCATTER) {
+                    if (static_cast<int>(sub) < K) dst[u][0] = __ldg(row_of + r * K + sub);
+                    if (static_cast<int>(sub) + 8 < K) dst[u][1] = __ldg(row_of + r * K + 8 + sub);
+                }
             }
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const float v0 = bf16_lo(w[u].x), v1 = bf16_hi(w[u].x), v2 = bf16_lo(w[u].y), v3 = bf16_hi(w[u].y);
-            const float v4 = bf16_lo(w[u].z), v5 = bf16_hi(w[u].z), v6 = bf16_lo(w[u].w), v7 = bf16_hi(w[u].w);
-            float amax = fmaxf(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))),
-                               fmaxf(fmaxf(fabsf(v4), fabsf(v5)), fmaxf(fabsf(v6), fabsf(v7))));
+            float v[16];
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            for (int h = 0; h < 2; ++h) {
+                v[8 * h + 0] = bf16_lo(w[u][h].x); v[8 * h + 1] = bf16_hi(w[u][h].x);
+                v[8 * h + 2] = bf16_lo(w[u][h].y); v[8 * h + 3] = bf16_hi(w[u][h].y);
+                v[8 * h + 4] = bf16_lo(w[u][h].z); v[8 * h + 5] = bf16_hi(w[u][h].z);
+                v[8 * h + 6] = bf16_lo(w[u][h].w); v[8 * h + 7] = bf16_hi(w[u][h].w);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             const float s = tile_scale<POW2>(amax);
-            uint2 codes;
-            codes.x = e4m3x4(quant_ratio(v0, s), quant_ratio(v1, s), quant_ratio(v2, s), quant_ratio(v3, s));
-            codes.y = e4m3x4(quant_ratio(v4, s), quant_ratio(v5, s), quant_ratio(v6, s), quant_ratio(v7, s));
+            uint4 codes;
+            codes.x = e4m3x4(quant_ratio(v[0], s), quant_ratio(v[1], s), quant_ratio(v[2], s), quant_ratio(v[3], s));
+            codes.y = e4m3x4(quant_ratio(v[4], s), quant_ratio(v[5], s), quant_ratio(v[6], s), quant_ratio(v[7], s));
+            codes.z = e4m3x4(quant_ratio(v[8], s), quant_ratio(v[9], s), quant_ratio(v[10], s), quant_ratio(v[11], s));
+            codes.w = e4m3x4(quant_ratio(v[12], s), quant_ratio(v[13], s), quant_ratio(v[14], s),
+                             quant_ratio(v[15], s));
             const int64_t r = tile[u] / tiles_per_row, c = tile[u] - r * tiles_per_row;
             if (!SCATTER) {
                 if (!live[u]) continue;
-                reinterpret_cast<uint2*>(q + r * cols + c * 128)[sub] = codes;
+                reinterpret_cast<uint4*>(q + r * cols + c * 128)[sub] = codes;
                 if (sub == 0) scale[r * tiles_per_row + c] = s;
             } else {
                 // every lane of the warp takes part in the shuffles, live or not
                 const int64_t routed = rows * K;
                 for (int k = 0; k <= K; ++k) {
-                    int64_t row = k < K ? __shfl_sync(0xffffffffu, dst[u], (lane & 16) + k) : routed + r;
+                    const int from = __shfl_sync(0xffffffffu, k < 8 ? dst[u][0] : dst[u][1], base + (k & 7));
+                    const int64_t row = k < K ? static_cast<int64_t>(from) : routed + r;
                     if (!live[u]) continue;
                     if (k < K && (row < 0 || row >= routed)) {
                         if (sub == 0) set_status(MOE_ERR_DEVICE_CHECK);
                         continue;
                     }
-                    reinterpret_cast<uint2*>(q + row * cols + c * 128)[sub] = codes;
+                    reinterpret_cast<uint4*>(q + row * cols + c * 128)[sub] = codes;
                     if (sub == 0) scale[row * tiles_per_row + c] = s;
                 }
             }

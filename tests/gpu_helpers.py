@@ -60,8 +60,10 @@ def assert_y_close(got, want, budget=None, name="y"):
         material = float(np.mean(budget > 1e-3 * rms))
         msg += (f"; beyond the E4M3-decision budget max-abs/RMS {mx:.3e}; budget {share:.2e} of the output, "
                 f"above 1e-3 RMS on {material:.2%} of elements")
+        print(msg)
         assert share <= BUDGET_CAP, f"{name}: budget {share:.3e} of the output"
-    print(msg)
+    else:
+        print(msg)
     assert rel <= Y_REL_L2, f"{name}: rel-L2 {rel:.3e}"
     assert mx <= Y_MAX_RMS, f"{name}: max-abs/RMS {mx:.3e}"
     return rel, mx

@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 
 from oracle import e4m3
-from oracle.bounds import GEMM_C, U
+from oracle.bounds import CHUNK_ROUNDINGS, U
 from oracle.backward import (Quantiser, dequant_128x1_grouped, gate_grad, gemm_bound, gemm_fp8_wgrad,
                              layer_backward, quant_128x1_grouped, segment_starts, swiglu_grad)
 
@@ -216,26 +216,37 @@ def test_quantiser_range_at_and_away_from_rounding_midpoints():
 
 
 def test_gemm_bound_covers_float32_chunked_evaluation():
-    """gemm_bound against a float32 evaluation written out the way a chunk-promoted GEMM
-    works (float32 chunk partial sums, float32 promotion per chunk): the float32 result lies
-    within the bound of the exact product, and the bound is not vacuous (a few per cent of
-    it is used on some element)."""
+    """gemm_bound against FP32 evaluations written out the way a chunk-promoted GEMM works:
+    each 128-element chunk summed in four FP32 steps of 32 exact products (in two different
+    orders), then promoted into an FP32 running sum. Every result lies within the bound of
+    the exact product; the bound is not vacuous (a sizeable part of it is used somewhere);
+    and it is the stated formula."""
     rng = np.random.default_rng(8)
     m, k, n = 16, 1024, 24
     A = (rng.standard_normal((m, k)) * np.exp(rng.uniform(-3, 3, (m, k)))).astype(np.float32).astype(np.float64)
     B = rng.standard_normal((k, n)).astype(np.float32).astype(np.float64)
     exact = A @ B
-    acc = np.zeros((m, n), np.float32)
-    for c in range(k // 128):
-        part = np.zeros((m, n), np.float32)
-        for j in range(c * 128, (c + 1) * 128):
-            part = (part + (A[:, j:j + 1] * B[j:j + 1, :]).astype(np.float32)).astype(np.float32)
-        acc = (acc + part).astype(np.float32)
-    bound = gemm_bound(A, B, k // 128)
-    err = np.abs(acc.astype(np.float64) - exact)
-    assert (err <= bound).all()
-    assert (err / bound).max() > 0.01
-    assert np.allclose(bound, (k // 128 + GEMM_C) * U * (np.abs(A) @ np.abs(B)))
+    bound = gemm_bound(A, B)
+    used = 0.0
+    for order in (1, -1):
+        acc = np.zeros((m, n), np.float32)
+        for c in range(k // 128):
+            part = np.zeros((m, n), np.float32)
+            for step in range(4)[::order]:
+                cols = slice(c * 128 + 32 * step, c * 128 + 32 * step + 32)
+                part = (part + (A[:, cols] @ B[cols]).astype(np.float32)).astype(np.float32)
+            acc = (acc + part).astype(np.float32)
+        err = np.abs(acc.astype(np.float64) - exact)
+        assert (err <= bound).all()
+        used = max(used, float((err / bound).max()))
+    assert used > 0.05
+    run = np.zeros((m, n))
+    acc = np.zeros((m, n))
+    for c in range(0, k, 128):
+        p = A[:, c:c + 128] @ B[c:c + 128]
+        acc += p
+        run += np.abs(p) + np.abs(acc)
+    assert np.allclose(bound, U * (CHUNK_ROUNDINGS * (np.abs(A) @ np.abs(B)) + run))
 
 
 def _planted_case(plant):
