@@ -14,11 +14,13 @@ bound, so the bounds here are derived from the arithmetic:
   lies within u * (CHUNK_ROUNDINGS * sum|terms| + sum over chunks of
   (|f P| + |acc|)) of the exact sum (u = 2^-24, first order). Inside a chunk
   the tensor core adds four K=32 steps of exact E4M3 products into an FP32
-  accumulator, each rounding once on a partial sum no larger than the chunk's
-  sum of |terms|; the promotion rounds the chunk's scale product (|f P|) and
+  accumulator; how a step aligns its 32 products is not documented, so each
+  step may round up to four times on partial sums no larger than the chunk's
+  sum of |terms|. The promotion rounds the chunk's scale product (|f P|) and
   its fused multiply-add into the running sum (|acc| after the chunk), both
   evaluated from the exact partial sums. Pinned against the device's
-  FP32-output GEMMs by GPU tests.
+  FP32-output GEMMs by GPU tests, on layer-like operands and on random codes
+  over the whole E4M3 range.
 * elementwise FP32 chains (SiLU and its gradient) add a few ulps (ARITH_ULPS;
   FAST_ULPS for the forward's fast exponential and division), and first-order
   sensitivities carry input bounds through them.
@@ -40,7 +42,9 @@ from . import e4m3
 from .quant import TILE, dequant_1x128, quant_1x128, tile_scale
 
 U = 2.0 ** -24           # unit roundoff of FP32 (round to nearest)
-CHUNK_ROUNDINGS = 4      # K=32 tensor-core steps per 128-element chunk, one rounding each
+CHUNK_ROUNDINGS = 16     # roundings inside one 128-element chunk: four K=32 tensor-core steps, each
+                         # aligning 32 exact products into the accumulator (its internal alignment is
+                         # not documented: four roundings of the step's sum of |terms| are allowed)
 ARITH_ULPS = 8           # an elementwise FP32 chain with exp and division (SiLU, its gradient)
 FAST_ULPS = 16           # the same with the fast exponential and division
 ROUTER_LOGIT_ERR = 1e-5  # |router logit - exact| of a correct FP32 router at these widths
@@ -85,18 +89,19 @@ def silu_derivs(a):
 
 def tile_range(v, err, rule: str = "fp32"):
     """[lo, hi] per element of the dequantised values of v under the 1x128 rule along the
-    last axis when each element may be off by up to err (and its tile's amax by up to the
-    tile's largest err): the four corner evaluations, value low/high x amax low/high."""
+    last axis when each element may be off by up to err: the four corner evaluations, value
+    low/high x tile amax low/high (the amax's own interval from every element's)."""
     v = np.asarray(v, np.float64)
     err = np.broadcast_to(np.asarray(err, np.float64), v.shape)
     rows, cols = v.shape
     t = v.reshape(rows, cols // TILE, TILE)
     et = err.reshape(rows, cols // TILE, TILE)
-    amax = np.abs(t).max(axis=2)
-    eamax = et.max(axis=2)
+    # the tile amax of any evaluation within err lies in [max(|v| - err), max(|v| + err)]
+    am_lo = np.maximum(np.abs(t) - et, 0.0).max(axis=2)
+    am_hi = (np.abs(t) + et).max(axis=2)
     outs = []
     for vs in (t - et, t + et):
-        for am in (np.maximum(amax - eamax, 0.0), amax + eamax):
+        for am in (am_lo, am_hi):
             sc = tile_scale(am.astype(np.float32), rule).astype(np.float64)
             scb = np.broadcast_to(sc[:, :, None], t.shape)
             with np.errstate(divide="ignore", invalid="ignore"):

@@ -17,8 +17,7 @@
 // One CTA per (128-token tile, <=256-expert tile, K slice); a K slice is a
 // contiguous range of sub-splits, more than one only to fill the SMs when
 // the batch is small:
-//   warp 0      TMA: x (128x64 bf16) once per k block into a 3-slot ring, and
-//               one weight term (BNx64 bf16) per chunk into a 4-slot ring
+//   warp 0      TMA: x (128x64 bf16) and one weight term (BNx64 bf16) per chunk
 //   warp 1      MMA: 4 x tcgen05.mma.kind::f16 (K=16) per chunk
 //   warps 2..9  sum the sub-splits, 128 logits per thread (lane quadrant =
 //               warp % 4, column half = (warp - 2) / 4)
@@ -39,16 +38,14 @@ namespace rtc {
 constexpr int BM = 128;
 constexpr int BK = 64;                 // bf16 elements per 128-byte row
 constexpr int BN_MAX = 256;
-constexpr int A_STAGES = 3;            // x tiles: one per k block, shared by its three weight terms
-constexpr int B_STAGES = 4;            // weight-term tiles: one per chunk
+constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN_MAX * BK * 2;
-constexpr int RING_BYTES = A_STAGES * A_BYTES + B_STAGES * B_BYTES;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 #ifndef MOE_ROUTE_MAX_CHUNKS
 #define MOE_ROUTE_MAX_CHUNKS 3
 #endif
 constexpr int kMaxChunksPerSplit = MOE_ROUTE_MAX_CHUNKS;   // chunks of 64 per TMEM accumulation run
-static_assert(kMaxChunksPerSplit % 3 == 0, "runs cover whole k blocks (three weight terms each)");
 constexpr int kMaxSlices = 16;                              // K slices across CTAs (small batches)
 
 constexpr int F_THREADS = 320;
@@ -57,14 +54,12 @@ constexpr int F_LD = BN_MAX + 4;                    // staged logit row stride (
 constexpr uint32_t F_TMEM_COLS = 2 * BN_MAX;
 constexpr size_t F_LOGIT_BYTES = static_cast<size_t>(BM) * F_LD * sizeof(float);
 constexpr size_t F_SEL_BYTES = static_cast<size_t>(F_WARPS) * 2 * BN_MAX * sizeof(float);
-static_assert(F_LOGIT_BYTES + F_SEL_BYTES <= static_cast<size_t>(RING_BYTES),
-              "staged logits and selection rows must fit in the operand rings");
+static_assert(F_LOGIT_BYTES + F_SEL_BYTES <= static_cast<size_t>(STAGES) * STAGE_BYTES,
+              "staged logits and selection rows must fit in the operand ring");
 
 struct FSmem {
-    uint64_t afull[A_STAGES];
-    uint64_t aempty[A_STAGES];
-    uint64_t full[B_STAGES];
-    uint64_t empty[B_STAGES];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t done;
@@ -72,7 +67,7 @@ struct FSmem {
     int abort;
 };
 
-constexpr size_t F_SMEM_BYTES = 1024 + RING_BYTES + sizeof(FSmem);
+constexpr size_t F_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + sizeof(FSmem);
 
 // Wr (FP32) -> three bf16 planes [3][E][d] with hi + mid + lo == Wr.
 __global__ void split_kernel(const float* __restrict__ w, int64_t n, uint16_t* __restrict__ planes) {
@@ -106,8 +101,8 @@ route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = base;
-    uint8_t* sB = base + A_STAGES * A_BYTES;
-    FSmem& s = *reinterpret_cast<FSmem*>(base + RING_BYTES);
+    uint8_t* sB = base + STAGES * A_BYTES;
+    FSmem& s = *reinterpret_cast<FSmem*>(base + STAGES * STAGE_BYTES);
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
     const int t0 = blockIdx.x * BM;
@@ -120,8 +115,7 @@ route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     const int nsub = (c_end - c_begin + kMaxChunksPerSplit - 1) / kMaxChunksPerSplit;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < A_STAGES; ++i) { mbar_init(&s.afull[i], 1); mbar_init(&s.aempty[i], 1); }
-        for (int i = 0; i < B_STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
+        for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&s.tfull[i], 1); mbar_init(&s.tempty[i], 8); }
         mbar_init(&s.done, 1);
         s.abort = 0;
@@ -142,65 +136,45 @@ route_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CU
     volatile int* abort = &s.abort;
     // the weight box is min(E, 256) rows for every expert tile (a last tile narrower
     // than the box still receives, and counts, the whole box)
-    const uint32_t tx_b = static_cast<uint32_t>(min(E, BN_MAX)) * BK * 2;
+    const uint32_t tx_bytes = A_BYTES + static_cast<uint32_t>(min(E, BN_MAX)) * BK * 2;
 
     float acc[128];                                      // summing warps: this thread's 128 logits
     if (warp == 0) {
         if (lane == 0) {
-            // chunk c = 3 kb + term: the x tile of k block kb is loaded once, before its first
-            // term, into the A ring; each term's weight tile into the B ring
-            uint32_t it = 0, ia = 0;
-            bool ok = true;
-            for (int c = c_begin; c < c_end && ok; ++c, ++it) {
+            uint32_t it = 0;
+            for (int c = c_begin; c < c_end; ++c, ++it) {
+                const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
+                if (!mbar_wait(&s.empty[st], ph ^ 1u, abort, kWaitLimitNs)) break;
                 const int kb = c / 3, term = c - 3 * kb;
-                if (term == 0) {
-                    const uint32_t st = ia % A_STAGES, ph = (ia / A_STAGES) & 1u;
-                    if (!mbar_wait(&s.aempty[st], ph ^ 1u, abort, kWaitLimitNs)) break;
-                    mbar_expect_tx(&s.afull[st], A_BYTES);
-                    tma_load_2d(sA + st * A_BYTES, &tmX, &s.afull[st], kb * BK, t0);
-                    ++ia;
-                }
-                const uint32_t st = it % B_STAGES, ph = (it / B_STAGES) & 1u;
-                if (!mbar_wait(&s.empty[st], ph ^ 1u, abort, kWaitLimitNs)) { ok = false; break; }
-                mbar_expect_tx(&s.full[st], tx_b);
+                mbar_expect_tx(&s.full[st], tx_bytes);
+                tma_load_2d(sA + st * A_BYTES, &tmX, &s.full[st], kb * BK, t0);
                 tma_load_2d(sB + st * B_BYTES, &tmW, &s.full[st], kb * BK, term * E + n0);
             }
             if (*abort) {      // let every issued copy land before the CTA moves on
-                for (uint32_t j = it > B_STAGES ? it - B_STAGES : 0; j < it; ++j)
-                    mbar_wait(&s.full[j % B_STAGES], (j / B_STAGES) & 1u, nullptr, kWaitLimitNs);
-                for (uint32_t j = ia > A_STAGES ? ia - A_STAGES : 0; j < ia; ++j)
-                    mbar_wait(&s.afull[j % A_STAGES], (j / A_STAGES) & 1u, nullptr, kWaitLimitNs);
+                const uint32_t first = it > STAGES ? it - STAGES : 0;
+                for (uint32_t j = first; j < it; ++j)
+                    mbar_wait(&s.full[j % STAGES], (j / STAGES) & 1u, nullptr, kWaitLimitNs);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = make_idesc(BM, static_cast<uint32_t>(bn), 1);
-            uint32_t it = 0, ia = 0;
+            uint32_t it = 0;
             bool ok = true;
             for (int sp = 0; sp < nsub && ok; ++sp) {
                 const uint32_t b = sp & 1, bph = (sp >> 1) & 1;
                 if (!mbar_wait(&s.tempty[b], bph ^ 1u, abort, kWaitLimitNs)) break;
                 const int c0 = c_begin + sp * kMaxChunksPerSplit, c1 = min(c_end, c0 + kMaxChunksPerSplit);
                 for (int c = c0; c < c1; ++c, ++it) {
-                    const int term = c % 3;
-                    const uint32_t sa = ia % A_STAGES;
-                    if (term == 0 && !mbar_wait(&s.afull[sa], (ia / A_STAGES) & 1u, abort, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t st = it % B_STAGES, ph = (it / B_STAGES) & 1u;
+                    const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
                     if (!mbar_wait(&s.full[st], ph, abort, kWaitLimitNs)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t ad = sw128_desc(smem_addr(sA + sa * A_BYTES));
+                    const uint64_t ad = sw128_desc(smem_addr(sA + st * A_BYTES));
                     const uint64_t bd = sw128_desc(smem_addr(sB + st * B_BYTES));
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         mma_bf16(tmem + b * BN_MAX, ad + 2 * k, bd + 2 * k, idesc, (c > c0 || k > 0) ? 1u : 0u);
                     tc_commit(&s.empty[st]);
-                    if (term == 2) {                     // the k block's x tile has served its three terms
-                        tc_commit(&s.aempty[sa]);
-                        ++ia;
-                    }
                 }
                 if (ok) tc_commit(&s.tfull[b]);
             }

