@@ -610,7 +610,7 @@ def run_fp8_peak(args):
     """--fp8-peak: dense E4M3 GEMM throughput of the vendor library on this GPU (torch._scaled_mm,
     8192^3, per-tensor unit scales, bf16 output), best of 10 timed with CUDA events after 3
     warm-ups, with the SM clock sampled meanwhile. A measured context figure for the FP8
-    roofline denominators; the reported fractions keep the measured bf16 figure."""
+    roofline denominators; the reported fractions keep the bf16 figure of MEASURED_PEAKS.json."""
     import torch
     torch.cuda.set_device(0)
     n = 8192
