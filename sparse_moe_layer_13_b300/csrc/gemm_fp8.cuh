@@ -55,7 +55,7 @@ struct Smem {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t tempty[4];               // chunk it's TMEM buffer read out (index it % 4, one arrive per epilogue warp)
     uint64_t mma_done;
     uint64_t pair[4];                 // SwiGLU amax exchange between the two warps of a lane quadrant
     uint32_t tmem_base;
@@ -66,7 +66,7 @@ struct Smem {
     int mtile_prefix[MAX_GROUPS + 1]; // exclusive prefix of ceil(m_g / BM)
     float amax_x[2][8][32];
     uint2 tile_tab[TILE_TAB];         // this CTA's tiles in order: {g | nt << 11 | min(m_valid,128) << 19, row0}
-    float ring_sa[4][256];            // per-thread activation scale of chunks kc .. kc+3
+    alignas(16) float ring_sa[4][256];  // per-thread activation scale of chunks kc .. kc+3; VSC: per-warp weight scales
     float ring_sb[4][8][2];           // per-warp weight scales (two 128-column blocks)
 };
 
@@ -272,7 +272,11 @@ __device__ __forceinline__ void store_tile_tma(const float* acc, const Params& p
 
 // GATHER: A rows are fetched by index (TMA gather4, four rows per copy)
 // instead of as one 128-row tile.
-template <int EPI, bool GATHER>
+// VSC: the activation scales go straight from global memory into registers and a tile's
+// weight scales are staged once per tile (Kdim / 128 a multiple of 4 and at most 64, sa
+// and sb 16-byte aligned; not the all-FP32 epilogues) instead of streaming both through
+// the per-chunk shared-memory ring.
+template <int EPI, bool GATHER, bool VSC>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, Params p) {
@@ -293,7 +297,8 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
     // ---- set-up: barriers, TMEM, per-group row tiles -------------------------
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&s.tfull[i], 1); mbar_init(&s.tempty[i], 8); }
+        for (int i = 0; i < 2; ++i) mbar_init(&s.tfull[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&s.tempty[i], 8);
         mbar_init(&s.mma_done, 1);
         for (int i = 0; i < 4; ++i) mbar_init(&s.pair[i], 64);
         s.abort = 0;
@@ -405,8 +410,10 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
                 for (int kc = 0; kc < nkc; ++kc, ++it) {
                     const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
-                    const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-                    if (!mbar_wait(&s.tempty[b], bph ^ 1u, abort, kWaitLimitNs)) break;
+                    const uint32_t b = it & 1u;
+                    // buffer b is free once chunk it - 2 has been read out
+                    if (it >= 2 && !mbar_wait(&s.tempty[(it - 2) & 3u], ((it - 2) >> 2) & 1u, abort, kWaitLimitNs))
+                        break;
                     if (!mbar_wait(&s.full[st], ph, abort, kWaitLimitNs)) break;
                     tc_fence_after();
                     const uint64_t ad = sw128_desc(smem_addr(sA + st * A_BYTES));
@@ -459,15 +466,42 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 cp_async_4(&s.ring_sb[slot][ew][1], p.sb + rows.sb + (kSwigluLayout ? nkc : 0) + kc);
             }
         };
-        // hands chunk buffer b back to the MMA issuer once this warp's loads from it have
-        // completed (before the last half of the promotion arithmetic, which runs on registers)
-        auto release = [&](uint32_t b) {
+        // tells the MMA issuer that chunk position `it` has been read out of its TMEM buffer,
+        // once this warp's loads from it have completed (before the last half of the promotion
+        // arithmetic, which runs on registers)
+        auto release = [&](uint32_t it_done) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s.tempty[b]);
+            if (lane == 0) mbar_arrive(&s.tempty[it_done & 3u]);
         };
+        // VSC: the activation scales of this thread's row for K chunks 4j .. 4j+3 are one
+        // 16-byte load, issued one group of four chunks ahead (into the next tile at a tile's
+        // last group). A tile's weight scales (the warp's gate-block and up-block rows) are
+        // copied once per tile into a per-warp shared-memory row, while the previous tile is
+        // stored, and each chunk reads its pair with one broadcast load. (Per-chunk copies
+        // through the ring, shuffles from lane-held rows, and 16-byte weight-scale loads into
+        // registers all measured slower.)
+        auto a_row = [&](const TileInfo& t) -> const float* {
+            int64_t src_row = rit < t.m_valid ? static_cast<int64_t>(t.row0) + rit : 0;
+            if (GATHER && rit < t.m_valid) {
+                src_row = __ldg(p.row_index + src_row);
+                if (src_row < 0 || src_row >= p.a_rows) src_row = 0;      // reported by the producer
+            }
+            return p.sa + src_row * nkc;
+        };
+        float* wsb = &s.ring_sa[0][0] + ew * 128;     // this warp's weight scales: gate [0, nkc), up [64, 64 + nkc)
+        auto load_wscales = [&](const TileInfo& t) {
+            const float* g0 = p.sb + (static_cast<int64_t>(t.g) * nbn + 2 * t.nt + (kSwigluLayout ? 0 : half)) * nkc;
+            const int l = static_cast<int>(lane);
+            __syncwarp();
+            if (l < 16 && 4 * l < nkc) cp_async_16(wsb + 4 * l, g0 + 4 * l);
+            if (kSwigluLayout && l >= 16 && 4 * (l - 16) < nkc) cp_async_16(wsb + 64 + 4 * (l - 16), g0 + nkc + 4 * (l - 16));
+            cp_async_commit();
+        };
+        float4 a_cur = make_float4(0.0f, 0.0f, 0.0f, 0.0f), a_nxt = a_cur;
+        const float* arow_carry = p.sa;
         // (the all-FP32 store epilogue keeps per-tile copies: the look-ahead state makes it spill)
-        const bool ahead = EPI != MOE_EPI_F32 && EPI != MOE_EPI_GATEUP_F32 && nkc >= 3;
+        const bool ahead = !VSC && EPI != MOE_EPI_F32 && EPI != MOE_EPI_GATEUP_F32 && nkc >= 3;
         uint32_t it = 0, tcount = 0, nbox = 0;
         bool ok = true;
         ScaleRows cur{0, 0}, nxt{0, 0};
@@ -482,6 +516,11 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         const int last_start = s.row_start[groups - 1];
         TileInfo tnext = static_cast<int>(blockIdx.x) < total ? tile_info(s, groups, ntiles, 0, blockIdx.x)
                                                               : TileInfo{0, 0, 0, 0};
+        if (VSC && static_cast<int>(blockIdx.x) < total) {
+            arow_carry = a_row(tnext);
+            a_nxt = __ldg(reinterpret_cast<const float4*>(arow_carry));
+            load_wscales(tnext);
+        }
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
             const TileInfo t = tnext;
             const int g = t.g, nt = t.nt;
@@ -490,7 +529,10 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             const int next = tile + static_cast<int>(gridDim.x);
             const bool has_next = next < total;
             if (has_next) tnext = tile_info(s, groups, ntiles, static_cast<int>(tcount) + 1, next);
-            if (!ahead) {
+            const float* arow = arow_carry;                       // VSC: this tile's activation scales
+            const float* arow_next = arow;
+            if (VSC && has_next) arow_next = a_row(tnext);
+            if (!VSC && !ahead) {
                 cur = scale_rows(t);
                 for (int j = 0; j < 3; ++j) {
                     if (j < nkc) copy_scales(cur, j, (it + j) & 3u);
@@ -501,21 +543,38 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             float2 acc2[64];             // FP32 tile accumulator, column pairs
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+            if (VSC) {
+                cp_async_wait<0>();      // this tile's weight scales
+                __syncwarp();
+            }
             for (int kc = 0; kc < nkc; ++kc, ++it) {
                 const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-                cp_async_wait<2>();      // this position's copies were the oldest of three groups
-                __syncwarp();
-                const uint32_t slot = it & 3u;
-                const float sav = s.ring_sa[slot][et];
-                const float f0 = sav * s.ring_sb[slot][ew][0];
-                const float f1 = sav * s.ring_sb[slot][ew][1];
-                // three positions ahead: this tile, else (look-ahead) the next one
-                const int k3 = kc + 3;
-                if (k3 < nkc)
-                    copy_scales(cur, k3, (it + 3) & 3u);
-                else if (ahead && has_next)
-                    copy_scales(nxt, k3 - nkc, (it + 3) & 3u);
-                cp_async_commit();
+                float f0, f1;
+                if constexpr (VSC) {
+                    if ((kc & 3) == 0) {
+                        a_cur = a_nxt;
+                        const float* src = kc + 4 < nkc ? arow + kc + 4 : arow_next;
+                        a_nxt = __ldg(reinterpret_cast<const float4*>(src));
+                    }
+                    const int j = kc & 3;
+                    const float sav = j == 0 ? a_cur.x : j == 1 ? a_cur.y : j == 2 ? a_cur.z : a_cur.w;
+                    f0 = sav * wsb[kc];
+                    f1 = kSwigluLayout ? sav * wsb[64 + kc] : f0;
+                } else {
+                    cp_async_wait<2>();      // this position's copies were the oldest of three groups
+                    __syncwarp();
+                    const uint32_t slot = it & 3u;
+                    const float sav = s.ring_sa[slot][et];
+                    f0 = sav * s.ring_sb[slot][ew][0];
+                    f1 = sav * s.ring_sb[slot][ew][1];
+                    // three positions ahead: this tile, else (look-ahead) the next one
+                    const int k3 = kc + 3;
+                    if (k3 < nkc)
+                        copy_scales(cur, k3, (it + 3) & 3u);
+                    else if (ahead && has_next)
+                        copy_scales(nxt, k3 - nkc, (it + 3) & 3u);
+                    cp_async_commit();
+                }
                 // warp-uniform outcome: every lane leaves together (warp syncs follow)
                 if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[b], bph, abort, kWaitLimitNs))) { ok = false; break; }
                 tc_fence_after();
@@ -528,7 +587,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     tmem_ld_wait();
                     tmem_reg_fence(v0);
                     tmem_reg_fence(v1);
-                    if (r == 1) release(b);   // every value of the chunk is in registers now
+                    if (r == 1) release(it);   // every value of the chunk is in registers now
                     const float2 ff = make_float2((r == 0) ? f0 : f1, (r == 0) ? f0 : f1);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -541,6 +600,8 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             }
             float* acc = reinterpret_cast<float*>(acc2);
             if (!ok) break;
+            if (VSC && has_next) load_wscales(tnext);              // landed while the tile is stored
+            arow_carry = arow_next;
             if constexpr (EpiCfg<EPI>::kTmaOut)
                 store_tile_tma(acc, p, &tmOut, sOut, t, rit, half, ew, q, lane, nbox);
             else if (!store_tile<EPI, false>(acc, p, s, t, groups, last_start, rit, half, ew, q, lane, tcount, abort))

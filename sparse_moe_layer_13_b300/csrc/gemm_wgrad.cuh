@@ -49,7 +49,7 @@ struct Smem {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t tempty[4];                // chunk it's TMEM buffer read out (index it % 4, one arrive per epilogue warp)
     uint64_t sfull[SSLOTS];
     uint64_t sempty[SSLOTS];
     uint64_t mma_done;
@@ -103,7 +103,8 @@ grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&s.tfull[i], 1); mbar_init(&s.tempty[i], 8); }
+        for (int i = 0; i < 2; ++i) mbar_init(&s.tfull[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&s.tempty[i], 8);
         for (int i = 0; i < SSLOTS; ++i) { mbar_init(&s.sfull[i], 1); mbar_init(&s.sempty[i], 8); }
         mbar_init(&s.mma_done, 1);
         s.abort = 0;
@@ -194,8 +195,10 @@ grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             bool ok = true;
             for (int kc = 0; kc < nk; ++kc, ++it) {
                 const uint32_t st = it % STAGES, ph = (it / STAGES) & 1u;
-                const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-                if (!(ok = mbar_wait(&s.tempty[b], bph ^ 1u, abort, kWaitLimitNs))) break;
+                const uint32_t b = it & 1u;
+                // buffer b is free once chunk it - 2 has been read out
+                if (it >= 2 && !(ok = mbar_wait(&s.tempty[(it - 2) & 3u], ((it - 2) >> 2) & 1u, abort, kWaitLimitNs)))
+                    break;
                 if (!(ok = mbar_wait(&s.full[st], ph, abort, kWaitLimitNs))) break;
                 tc_fence_after();
                 const uint64_t ad = sw128_desc(smem_addr(sA + st * A_BYTES));
@@ -247,7 +250,7 @@ grouped_wgrad_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     if (r == 3) {                // every value of the chunk is in registers now
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&s.tempty[b]);
+                        if (lane == 0) mbar_arrive(&s.tempty[it & 3u]);
                     }
                     const float4* sbp = reinterpret_cast<const float4*>(&s.sb[ss][half * 128 + r * 32]);
 #pragma unroll

@@ -240,16 +240,29 @@ moe_status launch_fused(const moe_config* c, const CUtensorMap& tx, const CUtens
 }
 
 // to: the FP32 output's tensor map for the all-FP32 epilogues (unused by the others)
+template <int EPI, bool GATHER, bool VSC>
+moe_status launch_gemm_v(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const gemm::Params& p,
+                         int64_t tiles_max, cudaStream_t st) {
+    constexpr size_t smem = gemm::EpiCfg<EPI>::kSmem;
+    static std::atomic<uint64_t> attr_done{0};
+    const void* fn = reinterpret_cast<const void*>(gemm::grouped_gemm_fp8_kernel<EPI, GATHER, VSC>);
+    if (smem_attr(fn, smem, attr_done) != MOE_OK) return MOE_ERR_CUDA;
+    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_max, 1)));
+    gemm::grouped_gemm_fp8_kernel<EPI, GATHER, VSC><<<grid, gemm::NUM_THREADS, smem, st>>>(ta, tb, to, p);
+    return launch_status();
+}
+
+// Chunk scales in registers (VSC) where the kernel supports it: K/128 a multiple of 4 and
+// at most 64, 16-byte aligned scale arrays, not an all-FP32 epilogue.
 template <int EPI, bool GATHER>
 moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const gemm::Params& p,
                        int64_t tiles_max, cudaStream_t st) {
-    constexpr size_t smem = gemm::EpiCfg<EPI>::kSmem;
-    static std::atomic<uint64_t> attr_done{0};
-    if (smem_attr(reinterpret_cast<const void*>(gemm::grouped_gemm_fp8_kernel<EPI, GATHER>), smem, attr_done) != MOE_OK)
-        return MOE_ERR_CUDA;
-    const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_max, 1)));
-    gemm::grouped_gemm_fp8_kernel<EPI, GATHER><<<grid, gemm::NUM_THREADS, smem, st>>>(ta, tb, to, p);
-    return launch_status();
+    if constexpr (EPI != MOE_EPI_F32 && EPI != MOE_EPI_GATEUP_F32) {
+        const int nkc = p.Kdim / gemm::BK;
+        if (nkc % 4 == 0 && nkc <= 64 && aligned16(p.sa) && aligned16(p.sb))
+            return launch_gemm_v<EPI, GATHER, true>(ta, tb, to, p, tiles_max, st);
+    }
+    return launch_gemm_v<EPI, GATHER, false>(ta, tb, to, p, tiles_max, st);
 }
 
 template <bool GATHER>

@@ -281,3 +281,51 @@ def test_gemm_f32_within_evaluation_bound(K):
         worst = max(worst, float(ratio.max()))
         assert (ratio <= 1.0).all(), f"group {g}: {int((ratio > 1).sum())} outputs beyond the bound"
     print(f"[bound] K={K}: worst |error| / gemm_bound = {worst:.3f}")
+
+
+def _off16(t):
+    """The same values in a buffer whose first element sits 4 bytes past a 16-byte boundary."""
+    flat = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = flat[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@gpu
+@pytest.mark.parametrize("K", [512, 1024, 7168, 8704])
+@pytest.mark.parametrize("epi", ["bf16", "swiglu", "bf16_f32_last"])
+@pytest.mark.parametrize("gather", [False, True])
+def test_gemm_scale_paths_agree(K, epi, gather):
+    """The chunk scales reach the promotion either from registers plus a weight-scale row
+    staged once per tile (16-byte aligned scale arrays, K/128 a multiple of 4 and at most 64)
+    or through the per-chunk shared-memory ring (every other case). Both take the same FP32
+    products in the same order, so the outputs agree bit for bit; scale arrays 4 bytes off a
+    16-byte boundary force the ring. K = 8704 (68 chunks) takes the ring either way."""
+    require_gpu()
+    from sparse_moe_layer_13_b300 import binding
+    sizes = [700, 300, 1000, 0, 257, 129, 513]
+    N = 512
+    offsets, A, sa, B, sb = _problem(sizes, N, K, seed=K + len(epi) + gather, trailing=5)
+    rng = np.random.default_rng(K)
+    rows = int(offsets[-1])
+    ridx = _row_index(rng, rows, A.shape[0]) if gather else None
+    o_d, A_d, sa_d, B_d, sb_d = _cuda(offsets, A, sa, B, sb)
+    ri_d = _cuda(ridx)[0] if gather else None
+    G = len(sizes)
+    last_rows = int(offsets[G] - offsets[G - 1])
+    outs = []
+    for sa_x, sb_x in ((sa_d, sb_d), (_off16(sa_d), _off16(sb_d))):
+        if epi == "swiglu":
+            out = torch.full((rows, N // 2), 0x55, dtype=torch.uint8, device="cuda")
+            aux = torch.full((rows, N // 256), -1.0, dtype=torch.float32, device="cuda")
+            code = binding.MOE_EPI_SWIGLU_FP8
+        else:
+            out = torch.full((rows, N), -7.0, dtype=torch.bfloat16, device="cuda")
+            aux = torch.full((last_rows, N), -7.0, dtype=torch.float32, device="cuda") if epi != "bf16" else None
+            code = binding.MOE_EPI_BF16 if epi == "bf16" else binding.MOE_EPI_BF16_F32_LAST
+        binding.grouped_gemm_fp8(o_d, A_d, sa_x, B_d, sb_x, code, out, aux, last_rows=last_rows, row_index=ri_d)
+        binding.check_device_status()
+        outs.append([to_np(out.view(torch.uint8) if out.dtype == torch.bfloat16 else out)] +
+                    ([to_np(aux)] if aux is not None else []))
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
