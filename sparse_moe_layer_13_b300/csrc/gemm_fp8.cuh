@@ -478,9 +478,13 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         // 16-byte load, issued one group of four chunks ahead (into the next tile at a tile's
         // last group). A tile's weight scales (the warp's gate-block and up-block rows) are
         // copied once per tile into a per-warp shared-memory row, while the previous tile is
-        // stored, and each chunk reads its pair with one broadcast load. (Per-chunk copies
-        // through the ring, shuffles from lane-held rows, and 16-byte weight-scale loads into
-        // registers all measured slower.)
+        // stored: SwiGLU layout interleaved, one 8-byte broadcast load per chunk; otherwise
+        // one 16-byte load per four chunks, a group ahead. Each per-chunk shared or shuffle
+        // instruction costs the epilogue warps beside the TMA and MMA warps about 40 cycles a
+        // chunk, so the number of such reads is what was minimised (per-chunk copies through the
+        // ring, shuffles from lane-held rows, separate gate and up loads, 16-byte register
+        // loads of the weight scales and, for the SwiGLU layout, 16-byte loads a pair of
+        // chunks ahead all measured slower).
         auto a_row = [&](const TileInfo& t) -> const float* {
             int64_t src_row = rit < t.m_valid ? static_cast<int64_t>(t.row0) + rit : 0;
             if (GATHER && rit < t.m_valid) {
@@ -489,13 +493,18 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             }
             return p.sa + src_row * nkc;
         };
-        float* wsb = &s.ring_sa[0][0] + ew * 128;     // this warp's weight scales: gate [0, nkc), up [64, 64 + nkc)
+        // this warp's weight scales of the tile: SwiGLU layout (gate, up) of chunk kc at
+        // [2 kc, 2 kc + 1]; otherwise chunk kc at [kc]
+        float* wsb = &s.ring_sa[0][0] + ew * 128;
         auto load_wscales = [&](const TileInfo& t) {
             const float* g0 = p.sb + (static_cast<int64_t>(t.g) * nbn + 2 * t.nt + (kSwigluLayout ? 0 : half)) * nkc;
             const int l = static_cast<int>(lane);
             __syncwarp();
-            if (l < 16 && 4 * l < nkc) cp_async_16(wsb + 4 * l, g0 + 4 * l);
-            if (kSwigluLayout && l >= 16 && 4 * (l - 16) < nkc) cp_async_16(wsb + 64 + 4 * (l - 16), g0 + nkc + 4 * (l - 16));
+            if (kSwigluLayout) {
+                for (int e = l; e < 2 * nkc; e += 32) cp_async_4(wsb + e, g0 + (e & 1) * nkc + (e >> 1));
+            } else if (4 * l < nkc) {
+                cp_async_16(wsb + 4 * l, g0 + 4 * l);
+            }
             cp_async_commit();
         };
         float4 a_cur = make_float4(0.0f, 0.0f, 0.0f, 0.0f), a_nxt = a_cur;
@@ -543,9 +552,11 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             float2 acc2[64];             // FP32 tile accumulator, column pairs
 #pragma unroll
             for (int i = 0; i < 64; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+            float4 wcur = make_float4(0.0f, 0.0f, 0.0f, 0.0f), wnxt = wcur;
             if (VSC) {
                 cp_async_wait<0>();      // this tile's weight scales
                 __syncwarp();
+                if (!kSwigluLayout) wnxt = *reinterpret_cast<const float4*>(wsb);
             }
             for (int kc = 0; kc < nkc; ++kc, ++it) {
                 const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
@@ -558,8 +569,18 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                     }
                     const int j = kc & 3;
                     const float sav = j == 0 ? a_cur.x : j == 1 ? a_cur.y : j == 2 ? a_cur.z : a_cur.w;
-                    f0 = sav * wsb[kc];
-                    f1 = kSwigluLayout ? sav * wsb[64 + kc] : f0;
+                    if (kSwigluLayout) {          // (gate, up) of this chunk in one 8-byte load
+                        const float2 w = *reinterpret_cast<const float2*>(wsb + 2 * kc);
+                        f0 = sav * w.x;
+                        f1 = sav * w.y;
+                    } else {                      // chunks kc .. kc + 3 in one 16-byte load, a group ahead
+                        if (j == 0) {
+                            wcur = wnxt;
+                            if (kc + 4 < nkc) wnxt = *reinterpret_cast<const float4*>(wsb + kc + 4);
+                        }
+                        f0 = sav * (j == 0 ? wcur.x : j == 1 ? wcur.y : j == 2 ? wcur.z : wcur.w);
+                        f1 = f0;
+                    }
                 } else {
                     cp_async_wait<2>();      // this position's copies were the oldest of three groups
                     __syncwarp();
