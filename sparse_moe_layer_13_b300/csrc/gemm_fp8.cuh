@@ -274,8 +274,8 @@ __device__ __forceinline__ void store_tile_tma(const float* acc, const Params& p
 // instead of as one 128-row tile.
 // VSC: the activation scales go straight from global memory into registers and a tile's
 // weight scales are staged once per tile (Kdim / 128 a multiple of 4 and at most 64, sa
-// and sb 16-byte aligned; not the all-FP32 epilogues) instead of streaming both through
-// the per-chunk shared-memory ring.
+// and sb 16-byte aligned) instead of streaming both through the per-chunk shared-memory
+// ring.
 template <int EPI, bool GATHER, bool VSC>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

@@ -253,15 +253,13 @@ moe_status launch_gemm_v(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
 }
 
 // Chunk scales in registers (VSC) where the kernel supports it: K/128 a multiple of 4 and
-// at most 64, 16-byte aligned scale arrays, not an all-FP32 epilogue.
+// at most 64, 16-byte aligned scale arrays.
 template <int EPI, bool GATHER>
 moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const gemm::Params& p,
                        int64_t tiles_max, cudaStream_t st) {
-    if constexpr (EPI != MOE_EPI_F32 && EPI != MOE_EPI_GATEUP_F32) {
-        const int nkc = p.Kdim / gemm::BK;
-        if (nkc % 4 == 0 && nkc <= 64 && aligned16(p.sa) && aligned16(p.sb))
-            return launch_gemm_v<EPI, GATHER, true>(ta, tb, to, p, tiles_max, st);
-    }
+    const int nkc = p.Kdim / gemm::BK;
+    if (nkc % 4 == 0 && nkc <= 64 && aligned16(p.sa) && aligned16(p.sb))
+        return launch_gemm_v<EPI, GATHER, true>(ta, tb, to, p, tiles_max, st);
     return launch_gemm_v<EPI, GATHER, false>(ta, tb, to, p, tiles_max, st);
 }
 

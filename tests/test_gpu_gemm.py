@@ -293,7 +293,7 @@ def _off16(t):
 
 @gpu
 @pytest.mark.parametrize("K", [512, 1024, 7168, 8704])
-@pytest.mark.parametrize("epi", ["bf16", "swiglu", "bf16_f32_last"])
+@pytest.mark.parametrize("epi", ["bf16", "swiglu", "bf16_f32_last", "f32", "gateup_f32"])
 @pytest.mark.parametrize("gather", [False, True])
 def test_gemm_scale_paths_agree(K, epi, gather):
     """The chunk scales reach the promotion either from registers plus a weight-scale row
@@ -319,6 +319,10 @@ def test_gemm_scale_paths_agree(K, epi, gather):
             out = torch.full((rows, N // 2), 0x55, dtype=torch.uint8, device="cuda")
             aux = torch.full((rows, N // 256), -1.0, dtype=torch.float32, device="cuda")
             code = binding.MOE_EPI_SWIGLU_FP8
+        elif epi in ("f32", "gateup_f32"):
+            out = torch.full((rows, N), -7.0, dtype=torch.float32, device="cuda")
+            aux = None
+            code = binding.MOE_EPI_F32 if epi == "f32" else binding.MOE_EPI_GATEUP_F32
         else:
             out = torch.full((rows, N), -7.0, dtype=torch.bfloat16, device="cuda")
             aux = torch.full((last_rows, N), -7.0, dtype=torch.float32, device="cuda") if epi != "bf16" else None
