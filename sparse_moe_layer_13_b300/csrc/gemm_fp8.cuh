@@ -18,7 +18,13 @@
 //               requantisation of h.
 // The chunk accumulator is released as soon as its last TMEM load lands
 // (before the second half of the promotion FMAs), so the tensor cores run up
-// to two chunks ahead of the promotion arithmetic.
+// to two chunks ahead of the promotion arithmetic; the release barriers are
+// indexed by chunk position mod 4, so the issuer of chunk c waits on exactly
+// the release of chunk c - 2. The chunk scales reach the epilogue either from
+// registers (activation scales, 16-byte loads a group of four chunks ahead)
+// and a per-warp shared row of the tile's weight scales staged once per tile
+// (VSC), or through a per-chunk shared-memory ring; both form the same
+// products.
 //
 // Tiles: for each group, ceil(m_g / 128) row tiles x N/256 column tiles,
 // numbered group by group with the column tile fastest; CTA c takes tiles
