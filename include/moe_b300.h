@@ -321,7 +321,10 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const int32_t* topk_idx,
  * groups * N/128 * Kdim/128 below 2^32 (else MOE_ERR_UNSUPPORTED_SHAPE).
  * Rows outside every group are not written.
  * Runs on the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA
- * operand loads); no workspace. */
+ * operand loads); no workspace. With Kdim/128 a multiple of 4 and at most
+ * 64 and sa, sb 16-byte aligned the chunk scales are read into registers
+ * (the faster path); otherwise they stream through shared memory. Both give
+ * the same bits. */
 moe_status moe_grouped_gemm_fp8(int32_t groups, const int32_t* offsets, int64_t rows,
                                 int32_t N, int32_t Kdim,
                                 const uint8_t* A, const float* sa,
